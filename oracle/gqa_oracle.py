@@ -1,0 +1,252 @@
+"""Plain fp64 CPU oracle for the grouped-query attention (GQA) forward pass.
+
+TEST INFRASTRUCTURE ONLY. Nothing on the product path may import this module:
+the tests, the smoke check and the benchmark's CPU-baseline leg are its only
+callers. It shares no code, tables or helpers with the CUDA library.
+
+What it computes, and where the pages define it
+-----------------------------------------------
+* Scaled dot-product attention ``softmax(Q K^T / sqrt(d_k)) V``:
+  "Modern LLM architecture (1): GQA and RMSNorm" (zeeklog.com), section 2.1,
+  the Attention formula.
+* GQA: ``h_q`` query heads, ``g`` key/value heads, ``group_size = h_q // g``.
+  Every K/V head is duplicated ``group_size`` times along the head axis
+  (``repeat_interleave(group_size, dim=1)``) so that query head ``i`` reads
+  K/V head ``i // group_size``; scores are scaled by ``1/sqrt(head_dim)``,
+  masked entries set to ``-inf`` before the softmax, then multiplied by V:
+  same page, section 2.3, the GroupedQueryAttention code.  The index map is
+  stated again as ``kv_head_id = query_head_id // group_size`` in the
+  "Qwen, DeepSeek and LLaMA3 attention survey" (jsqmd.com), section 2.2.
+* KV cache: two tensors ``[batch, g, seq_len, d_head]`` that grow by
+  concatenation along the sequence axis, and a decode step in which one new
+  query token attends over every cached K/V row: "What is Grouped-Query
+  Attention" explainer (ijyty.com), section 2.1 and section 2.2 (second step),
+  section 3.2 (cache concat).
+
+Readings where the pages are silent (each listed in the design notes):
+* causal mask: key ``j`` is visible to query ``i`` iff ``j <= i + q_offset``
+  (``q_offset = 0`` when queries and keys cover the same positions);
+* dropout is the identity (inference);
+* a decode row with zero valid cache rows returns zeros and ``lse = -inf``;
+* ``append`` drops rows that would land past ``S_max`` and reports it.
+
+Everything here is the definition written out: one K/V duplication, one
+score matrix per (batch, head), one softmax, one product with V. No tiling,
+no online softmax, no fusion.
+
+Parity pins (tests/test_oracle_pins.py): PyTorch's library SDPA with
+``enable_gqa`` in fp64, brute-force loops on tiny inputs, the MHA (g = h_q)
+and MQA (g = 1, broadcast ``expand`` form) special cases, hand-derived
+closed-form fixtures under tests/golden/, and the invariants listed there.
+"""
+
+from __future__ import annotations
+
+import numpy as np
+
+# Status values reported by ``append``; they mirror the numbering the C
+# interface documents, written out here independently.
+APPEND_OK = 0
+APPEND_CACHE_FULL = 5
+
+
+# ---------------------------------------------------------------------------
+# bf16 <-> fp64 (exact definitions of the storage format)
+# ---------------------------------------------------------------------------
+
+def bf16_bits_to_f64(bits: np.ndarray) -> np.ndarray:
+    """Exact value of bf16 numbers given as their raw uint16 bit patterns.
+
+    bf16 is the upper half of an IEEE-754 binary32, so widening is a shift.
+    """
+    u32 = np.asarray(bits).astype(np.uint32) << np.uint32(16)
+    return u32.view(np.float32).astype(np.float64)
+
+
+def f32_to_bf16_bits(x: np.ndarray) -> np.ndarray:
+    """Round binary32 values to bf16 (round to nearest, ties to even).
+
+    Used only to state what a bf16 output must equal; NaN is not expected.
+    """
+    u = np.asarray(x, dtype=np.float32).view(np.uint32).astype(np.uint64)
+    lsb = (u >> np.uint64(16)) & np.uint64(1)
+    rounded = (u + np.uint64(0x7FFF) + lsb) >> np.uint64(16)
+    return rounded.astype(np.uint16)
+
+
+# ---------------------------------------------------------------------------
+# Building blocks of the definition
+# ---------------------------------------------------------------------------
+
+def head_map(h_q: int, g: int) -> np.ndarray:
+    """K/V head read by each query head: ``i // (h_q // g)``."""
+    if g <= 0 or h_q % g != 0:
+        raise ValueError("h_q must be a positive multiple of g")
+    group_size = h_q // g
+    return np.array([i // group_size for i in range(h_q)], dtype=np.int64)
+
+
+def _expand_kv(x: np.ndarray, group_size: int, axis: int) -> np.ndarray:
+    """Duplicate every K/V head ``group_size`` times, consecutively.
+
+    Same result as ``repeat_interleave(group_size, dim=head_axis)``: head
+    ``j`` becomes heads ``j*group_size .. j*group_size + group_size - 1``.
+    """
+    return np.repeat(x, group_size, axis=axis)
+
+
+def _visible(i: int, j: int, q_offset: int) -> bool:
+    """Causal visibility of key ``j`` to query row ``i``."""
+    return j <= i + q_offset
+
+
+def _softmax_rows(scores: np.ndarray):
+    """Row softmax; returns (P, row max, row sum of exp(s - max)).
+
+    Rows that are entirely ``-inf`` give P = 0 and sum 0.
+    """
+    m = np.max(scores, axis=-1, keepdims=True)
+    m_safe = np.where(np.isfinite(m), m, 0.0)
+    e = np.exp(scores - m_safe)
+    s = np.sum(e, axis=-1, keepdims=True)
+    p = np.divide(e, s, out=np.zeros_like(e), where=s > 0)
+    return p, m, s
+
+
+def _lse(m: np.ndarray, s: np.ndarray) -> np.ndarray:
+    """Natural-log sum-exp of a row from its max and its shifted sum."""
+    with np.errstate(divide="ignore"):
+        return np.where(s > 0, m + np.log(np.where(s > 0, s, 1.0)), -np.inf)
+
+
+# ---------------------------------------------------------------------------
+# Prefill
+# ---------------------------------------------------------------------------
+
+def attention_probs(q, k, causal: bool, scale: float, q_offset: int = 0):
+    """Attention weights P[b, h, i, j] (tiny inputs; used by invariant tests).
+
+    q: [B, Lq, h_q, d]; k: [B, Lk, g, d].
+    """
+    q = np.asarray(q, dtype=np.float64)
+    k = np.asarray(k, dtype=np.float64)
+    B, Lq, h_q, _ = q.shape
+    Lk, g = k.shape[1], k.shape[2]
+    group_size = h_q // g
+    out = np.zeros((B, h_q, Lq, Lk))
+    for b in range(B):
+        k_rep = _expand_kv(k[b], group_size, axis=1)  # [Lk, h_q, d]
+        for h in range(h_q):
+            s = (q[b, :, h, :] @ k_rep[:, h, :].T) * scale
+            if causal:
+                for i in range(Lq):
+                    for j in range(Lk):
+                        if not _visible(i, j, q_offset):
+                            s[i, j] = -np.inf
+            out[b, h], _, _ = _softmax_rows(s)
+    return out
+
+
+def prefill(q, k, v, causal: bool, scale: float, q_offset: int = 0):
+    """GQA prefill: ``O = softmax(Q K_rep^T * scale + mask) V_rep``.
+
+    q: [B, Lq, h_q, d]; k, v: [B, Lk, g, d] (the projection output layout
+    ``view(B, L, heads, d_head)``).  Returns (O [B, Lq, h_q, d] fp64,
+    lse [B, h_q, Lq] fp64, natural log).  With ``causal`` the query row ``i``
+    sits at key position ``i + q_offset``.
+    """
+    q = np.asarray(q, dtype=np.float64)
+    k = np.asarray(k, dtype=np.float64)
+    v = np.asarray(v, dtype=np.float64)
+    B, Lq, h_q, d = q.shape
+    Lk, g = k.shape[1], k.shape[2]
+    if h_q % g != 0:
+        raise ValueError("h_q must be a multiple of g")
+    group_size = h_q // g
+    if causal:
+        mask = np.zeros((Lq, Lk), dtype=bool)
+        for i in range(Lq):
+            for j in range(Lk):
+                mask[i, j] = not _visible(i, j, q_offset)
+    out = np.empty((B, Lq, h_q, d))
+    lse = np.empty((B, h_q, Lq))
+    for b in range(B):
+        # explicit per-head duplication of K and V, one batch element at a time
+        k_rep = _expand_kv(k[b], group_size, axis=1)  # [Lk, h_q, d]
+        v_rep = _expand_kv(v[b], group_size, axis=1)
+        for h in range(h_q):
+            s = (q[b, :, h, :] @ k_rep[:, h, :].T) * scale
+            if causal:
+                s[mask] = -np.inf
+            p, m, ssum = _softmax_rows(s)
+            out[b, :, h, :] = p @ v_rep[:, h, :]
+            lse[b, h, :] = _lse(m, ssum)[:, 0]
+    return out, lse
+
+
+# ---------------------------------------------------------------------------
+# Decode over a [B, g, S_max, d] KV cache
+# ---------------------------------------------------------------------------
+
+def decode(q, k_cache, v_cache, seq_lens, scale: float):
+    """One-token GQA decode over the cache.
+
+    q: [B, h_q, d]; k_cache, v_cache: [B, g, S_max, d]; seq_lens: [B] valid
+    rows per sequence. Row ``j`` of sequence ``b`` is visible iff
+    ``j < seq_lens[b]``. Returns (O [B, h_q, d], lse [B, h_q]).
+    """
+    q = np.asarray(q, dtype=np.float64)
+    k_cache = np.asarray(k_cache, dtype=np.float64)
+    v_cache = np.asarray(v_cache, dtype=np.float64)
+    B, h_q, d = q.shape
+    g = k_cache.shape[1]
+    group_size = h_q // g
+    out = np.zeros((B, h_q, d))
+    lse = np.full((B, h_q), -np.inf)
+    for b in range(B):
+        n = int(seq_lens[b])
+        if n <= 0:
+            continue
+        k_rep = _expand_kv(k_cache[b, :, :n, :], group_size, axis=0)  # [h_q, n, d]
+        v_rep = _expand_kv(v_cache[b, :, :n, :], group_size, axis=0)
+        for h in range(h_q):
+            s = (k_rep[h] @ q[b, h]) * scale  # [n]
+            p, m, ssum = _softmax_rows(s[None, :])
+            out[b, h] = (p @ v_rep[h])[0]
+            lse[b, h] = _lse(m, ssum)[0, 0]
+    return out, lse
+
+
+# ---------------------------------------------------------------------------
+# KV cache append
+# ---------------------------------------------------------------------------
+
+def append(k_cache, v_cache, seq_lens, k_new, v_new):
+    """Write T new tokens per sequence at the end of its valid rows.
+
+    k_cache, v_cache: [B, g, S_max, d] (any dtype; copied, not converted);
+    seq_lens: [B]; k_new, v_new: [B, T, g, d] (projection layout).
+    Token ``t`` of sequence ``b`` goes to cache row ``seq_lens[b] + t`` of
+    every K/V head -- the concatenation along the sequence axis.  Rows that
+    would land at or past ``S_max`` are dropped and the status becomes
+    APPEND_CACHE_FULL; the new length is ``min(seq_lens[b] + T, S_max)``.
+    Returns (k_cache', v_cache', seq_lens', status).
+    """
+    kc = np.array(k_cache, copy=True)
+    vc = np.array(v_cache, copy=True)
+    lens = np.array(seq_lens, copy=True).astype(np.int64)
+    B, g, S_max, _ = kc.shape
+    T = k_new.shape[1]
+    status = APPEND_OK
+    new_lens = lens.copy()
+    for b in range(B):
+        for t in range(T):
+            pos = int(lens[b]) + t
+            if pos >= S_max:
+                status = APPEND_CACHE_FULL
+                continue
+            for h in range(g):
+                kc[b, h, pos, :] = k_new[b, t, h, :]
+                vc[b, h, pos, :] = v_new[b, t, h, :]
+        new_lens[b] = min(int(lens[b]) + T, S_max)
+    return kc, vc, new_lens, status
