@@ -1,0 +1,238 @@
+// api.cu -- the C interface: host-side argument checks, TMA tensor-map
+// encoding and kernel launches. Every check runs before any CUDA call, so a
+// rejected call touches neither the device nor the stream.
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <cmath>
+#include <cstdint>
+
+#include "../../include/gqa.h"
+#include "launch.h"
+
+namespace {
+
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                   const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                   const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn load_encode_fn() {
+  void* p = nullptr;
+  cudaDriverEntryPointQueryResult q;
+  if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                       &q) != cudaSuccess ||
+      q != cudaDriverEntryPointSuccess) {
+    return nullptr;
+  }
+  return reinterpret_cast<EncodeTiledFn>(p);
+}
+
+EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = load_encode_fn();  // thread-safe one-time init
+  return fn;
+}
+
+// bf16 tensor map with the 128-byte swizzle; dims/strides innermost first,
+// strides in bytes for dims 1..rank-1. Out-of-range boxes read zeros.
+bool encode_bf16(CUtensorMap* m, int rank, const void* base, const cuuint64_t* dims,
+                 const cuuint64_t* strides, const cuuint32_t* box) {
+  EncodeTiledFn fn = encode_fn();
+  if (fn == nullptr) return false;
+  const cuuint32_t es[5] = {1, 1, 1, 1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, static_cast<cuuint32_t>(rank),
+            const_cast<void*>(base), dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
+            CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+bool aligned4(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 3u) == 0; }
+bool pow2(int x) { return x > 0 && (x & (x - 1)) == 0; }
+int log2i(int x) {
+  int r = 0;
+  while ((1 << r) < x) ++r;
+  return r;
+}
+bool scale_ok(float s) { return std::isfinite(s) && s > 0.f; }
+
+// Heads / group-size rules shared by prefill and decode.
+bool heads_ok(int h_q, int g, int d) {
+  if (h_q < 1 || g < 1 || h_q % g != 0) return false;
+  const int G = h_q / g;
+  if (!pow2(G) || G > 128) return false;
+  return d == 64 || d == 128;
+}
+
+constexpr long long kMaxElems = 1LL << 40;
+
+struct DecodeLayout {
+  int split_len, n_split;
+  size_t part_o_bytes, part_lse_off, total;
+};
+
+DecodeLayout decode_layout(int B, int h_q, int g, int d, int S_max) {
+  DecodeLayout l{};
+  l.split_len = gqa::decode_split_len(B, g, S_max);
+  l.n_split = (S_max + l.split_len - 1) / l.split_len;
+  const size_t rows = static_cast<size_t>(B) * h_q * l.n_split;
+  l.part_o_bytes = rows * d * sizeof(float);
+  l.part_lse_off = (l.part_o_bytes + 255) & ~static_cast<size_t>(255);
+  l.total = l.part_lse_off + rows * sizeof(float);
+  return l;
+}
+
+bool decode_shape_ok(int B, int h_q, int g, int d, int S_max) {
+  if (B < 1 || B > 65535 || S_max < 1 || !heads_ok(h_q, g, d)) return false;
+  const long long G = h_q / g;
+  if (static_cast<long long>(g) * ((G + 31) / 32) > 65535) return false;
+  if (static_cast<long long>(B) * g * S_max * d >= kMaxElems) return false;
+  if (static_cast<long long>(B) * g >= (1LL << 31)) return false;
+  return true;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* gqa_status_string(int status) {
+  switch (status) {
+    case GQA_OK: return "GQA_OK";
+    case GQA_ERR_NULL: return "GQA_ERR_NULL: a required pointer is NULL";
+    case GQA_ERR_SHAPE: return "GQA_ERR_SHAPE: size out of range or inconsistent";
+    case GQA_ERR_ALIGN: return "GQA_ERR_ALIGN: pointer not 16-byte aligned";
+    case GQA_ERR_WORKSPACE: return "GQA_ERR_WORKSPACE: workspace missing or too small";
+    case GQA_ERR_CACHE_FULL: return "GQA_ERR_CACHE_FULL: appended rows did not fit";
+    case GQA_ERR_CUDA: return "GQA_ERR_CUDA: a CUDA call or launch failed";
+    case GQA_ERR_TIMEOUT: return "GQA_ERR_TIMEOUT: a bounded wait inside a kernel ran out";
+    case GQA_ERR_BAD_LENGTH: return "GQA_ERR_BAD_LENGTH: a sequence length was out of range";
+    default: return "GQA_ERR_UNKNOWN";
+  }
+}
+
+int gqa_version(void) { return 100; }
+
+int gqa_prefill_fwd(const void* q, const void* k, const void* v, void* o, int o_dtype,
+                    float* lse, int B, int L, int h_q, int g, int d, float scale, int causal,
+                    int32_t* status_dev, void* stream) {
+  if (q == nullptr || k == nullptr || v == nullptr || o == nullptr) return GQA_ERR_NULL;
+  if (B < 1 || B > 65535 || L < 1 || !heads_ok(h_q, g, d) || g > 65535) return GQA_ERR_SHAPE;
+  if (o_dtype != GQA_OUT_F32 && o_dtype != GQA_OUT_BF16) return GQA_ERR_SHAPE;
+  if (!scale_ok(scale)) return GQA_ERR_SHAPE;
+  if (static_cast<long long>(B) * L * h_q * d >= kMaxElems) return GQA_ERR_SHAPE;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o)) return GQA_ERR_ALIGN;
+  if (lse != nullptr && !aligned4(lse)) return GQA_ERR_ALIGN;
+  if (status_dev != nullptr && !aligned4(status_dev)) return GQA_ERR_ALIGN;
+
+  const int G = h_q / g;
+  gqa::PrefillArgs a{};
+  const cuuint64_t e = 2;  // bytes per bf16
+  {
+    const cuuint64_t dims[4] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(h_q),
+                                static_cast<cuuint64_t>(L), static_cast<cuuint64_t>(B)};
+    const cuuint64_t strides[3] = {d * e, static_cast<cuuint64_t>(h_q) * d * e,
+                                   static_cast<cuuint64_t>(L) * h_q * d * e};
+    const cuuint32_t box[4] = {64, static_cast<cuuint32_t>(G),
+                               static_cast<cuuint32_t>(gqa::kPrefillBM / G), 1};
+    if (!encode_bf16(&a.tm_q, 4, q, dims, strides, box)) return GQA_ERR_CUDA;
+  }
+  {
+    const cuuint64_t dims[4] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(g),
+                                static_cast<cuuint64_t>(L), static_cast<cuuint64_t>(B)};
+    const cuuint64_t strides[3] = {d * e, static_cast<cuuint64_t>(g) * d * e,
+                                   static_cast<cuuint64_t>(L) * g * d * e};
+    const cuuint32_t box[4] = {64, 1, static_cast<cuuint32_t>(gqa::kPrefillBN), 1};
+    if (!encode_bf16(&a.tm_k, 4, k, dims, strides, box)) return GQA_ERR_CUDA;
+    if (!encode_bf16(&a.tm_v, 4, v, dims, strides, box)) return GQA_ERR_CUDA;
+  }
+  a.o = o;
+  a.o_dtype = o_dtype;
+  a.lse = lse;
+  a.B = B;
+  a.L = L;
+  a.h_q = h_q;
+  a.g = g;
+  a.d = d;
+  a.G = G;
+  a.G_log2 = log2i(G);
+  a.scale_log2 = scale * 1.4426950408889634f;
+  a.causal = causal != 0;
+  a.status = status_dev;
+  return gqa::launch_prefill(a, static_cast<cudaStream_t>(stream)) == cudaSuccess ? GQA_OK
+                                                                                    : GQA_ERR_CUDA;
+}
+
+size_t gqa_decode_workspace_bytes(int B, int h_q, int g, int d, int S_max) {
+  if (!decode_shape_ok(B, h_q, g, d, S_max)) return 0;
+  return decode_layout(B, h_q, g, d, S_max).total;
+}
+
+int gqa_decode_fwd(const void* q, const void* k_cache, const void* v_cache,
+                   const int32_t* seq_lens, void* o, int o_dtype, float* lse, int B, int h_q,
+                   int g, int d, int S_max, float scale, void* workspace, size_t workspace_bytes,
+                   int32_t* status_dev, void* stream) {
+  if (q == nullptr || k_cache == nullptr || v_cache == nullptr || seq_lens == nullptr ||
+      o == nullptr)
+    return GQA_ERR_NULL;
+  if (!decode_shape_ok(B, h_q, g, d, S_max)) return GQA_ERR_SHAPE;
+  if (o_dtype != GQA_OUT_F32 && o_dtype != GQA_OUT_BF16) return GQA_ERR_SHAPE;
+  if (!scale_ok(scale)) return GQA_ERR_SHAPE;
+  const DecodeLayout lay = decode_layout(B, h_q, g, d, S_max);
+  if (workspace == nullptr || workspace_bytes < lay.total) return GQA_ERR_WORKSPACE;
+  if (!aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(o) ||
+      !aligned16(workspace) || !aligned4(seq_lens))
+    return GQA_ERR_ALIGN;
+  if (lse != nullptr && !aligned4(lse)) return GQA_ERR_ALIGN;
+  if (status_dev != nullptr && !aligned4(status_dev)) return GQA_ERR_ALIGN;
+
+  gqa::DecodeArgs a{};
+  const cuuint64_t e = 2;
+  const cuuint64_t dims[3] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(S_max),
+                              static_cast<cuuint64_t>(B) * g};
+  const cuuint64_t strides[2] = {d * e, static_cast<cuuint64_t>(S_max) * d * e};
+  const cuuint32_t box[3] = {64, static_cast<cuuint32_t>(gqa::kDecodeStage), 1};
+  if (!encode_bf16(&a.tm_k, 3, k_cache, dims, strides, box)) return GQA_ERR_CUDA;
+  if (!encode_bf16(&a.tm_v, 3, v_cache, dims, strides, box)) return GQA_ERR_CUDA;
+  a.q = q;
+  a.seq_lens = seq_lens;
+  a.o = o;
+  a.o_dtype = o_dtype;
+  a.lse = lse;
+  a.part_o = static_cast<float*>(workspace);
+  a.part_lse = reinterpret_cast<float*>(static_cast<char*>(workspace) + lay.part_lse_off);
+  a.B = B;
+  a.h_q = h_q;
+  a.g = g;
+  a.d = d;
+  a.G = h_q / g;
+  a.S_max = S_max;
+  a.split_len = lay.split_len;
+  a.n_split = lay.n_split;
+  a.scale_log2 = scale * 1.4426950408889634f;
+  a.status = status_dev;
+  return gqa::launch_decode(a, static_cast<cudaStream_t>(stream)) == cudaSuccess ? GQA_OK
+                                                                                   : GQA_ERR_CUDA;
+}
+
+int kv_cache_append(void* k_cache, void* v_cache, int32_t* seq_lens, const void* k_new,
+                    const void* v_new, int B, int g, int d, int S_max, int T,
+                    int32_t* status_dev, void* stream) {
+  if (k_cache == nullptr || v_cache == nullptr || seq_lens == nullptr || k_new == nullptr ||
+      v_new == nullptr)
+    return GQA_ERR_NULL;
+  if (B < 1 || g < 1 || (d != 64 && d != 128) || S_max < 1 || T < 0) return GQA_ERR_SHAPE;
+  if (static_cast<long long>(B) * g * S_max * d >= kMaxElems ||
+      static_cast<long long>(B) * T * g * d >= kMaxElems)
+    return GQA_ERR_SHAPE;
+  if (!aligned16(k_cache) || !aligned16(v_cache) || !aligned16(k_new) || !aligned16(v_new) ||
+      !aligned4(seq_lens))
+    return GQA_ERR_ALIGN;
+  if (status_dev != nullptr && !aligned4(status_dev)) return GQA_ERR_ALIGN;
+  if (T == 0) return GQA_OK;
+  return gqa::launch_append(k_cache, v_cache, seq_lens, k_new, v_new, B, g, d, S_max, T,
+                            status_dev, static_cast<cudaStream_t>(stream)) == cudaSuccess
+             ? GQA_OK
+             : GQA_ERR_CUDA;
+}
+
+}  // extern "C"

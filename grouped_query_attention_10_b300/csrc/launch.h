@@ -1,0 +1,53 @@
+// launch.h -- host-side launchers shared between the kernel files and the
+// C interface (api.cu). Arguments are already validated when these run.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cstddef>
+#include <cstdint>
+
+namespace gqa {
+
+// Rows of one prefill query tile (TMEM lanes) and keys per K/V tile.
+constexpr int kPrefillBM = 128;
+constexpr int kPrefillBN = 128;
+
+// Tokens per decode pipeline stage.
+constexpr int kDecodeStage = 64;
+
+struct PrefillArgs {
+  CUtensorMap tm_q, tm_k, tm_v;
+  void* o;
+  int o_dtype;
+  float* lse;
+  int B, L, h_q, g, d, G, G_log2;
+  float scale_log2;  // softmax scale * log2(e)
+  int causal;
+  int32_t* status;
+};
+
+struct DecodeArgs {
+  CUtensorMap tm_k, tm_v;
+  const void* q;
+  const int32_t* seq_lens;
+  void* o;
+  int o_dtype;
+  float* lse;
+  float* part_o;    // [B, h_q, n_split, d]
+  float* part_lse;  // [B, h_q, n_split] (log2 units of the scaled scores)
+  int B, h_q, g, d, G, S_max, split_len, n_split;
+  float scale_log2;
+  int32_t* status;
+};
+
+cudaError_t launch_prefill(const PrefillArgs& a, cudaStream_t s);
+cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t s);
+cudaError_t launch_append(void* k_cache, void* v_cache, int32_t* seq_lens, const void* k_new,
+                          const void* v_new, int B, int g, int d, int S_max, int T,
+                          int32_t* status, cudaStream_t s);
+
+// Split length (tokens per split-KV CTA) used for these decode sizes.
+int decode_split_len(int B, int g, int S_max);
+
+}  // namespace gqa

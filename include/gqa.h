@@ -1,0 +1,146 @@
+/*
+ * gqa.h -- C interface of the B300 (sm_103a) grouped-query attention library.
+ *
+ * Grouped-query attention (GQA): h_q query heads share g key/value heads;
+ * query head i reads K/V head i / (h_q / g) (integer division), and each
+ * (batch, query head) computes softmax(Q K^T * scale) V. Sources: the
+ * GroupedQueryAttention code and the attention formula in "Modern LLM
+ * architecture (1): GQA and RMSNorm" (zeeklog.com), sections 2.1 and 2.3;
+ * the index map kv_head_id = query_head_id // group_size in the "Qwen,
+ * DeepSeek and LLaMA3 attention survey" (jsqmd.com), section 2.2; the KV
+ * cache layout [batch, g, seq_len, d_head] and its growth by concatenation in
+ * the "What is Grouped-Query Attention" explainer (ijyty.com), sections 2.2
+ * and 3.2.
+ *
+ * Conventions for every entry point
+ *  - All tensor pointers are DEVICE pointers owned by the caller, dense and
+ *    row-major in the layout stated, 16-byte aligned. The library never
+ *    allocates, frees or synchronises; work is queued on `stream` (a
+ *    cudaStream_t passed as void*, NULL = the legacy default stream).
+ *  - bf16 means IEEE bfloat16 (the upper 16 bits of a binary32).
+ *  - Arguments are checked on the host before anything is launched; a
+ *    failed check returns its status and queues no work.
+ *  - `status_dev` (optional, may be NULL) is a device int32 the kernels set
+ *    to a nonzero gqa_status_t when they detect a problem at run time
+ *    (a bounded wait that ran out, an append that did not fit). The first
+ *    problem recorded wins; the caller clears it and reads it after the
+ *    stream has been synchronised.
+ *  - Supported shapes: d in {64, 128}; g >= 1 divides h_q; the group size
+ *    G = h_q / g is a power of two no larger than 128; all sizes >= 1
+ *    (prefill) and their products fit the index types (B*L*h_q*d < 2^31,
+ *    B*g*S_max < 2^31).
+ *  - Kernels are built for sm_103a only; another device yields GQA_ERR_CUDA.
+ */
+#ifndef GQA_B300_H
+#define GQA_B300_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  GQA_OK = 0,
+  GQA_ERR_NULL = 1,        /* a required pointer is NULL                          */
+  GQA_ERR_SHAPE = 2,       /* a size is out of range or inconsistent              */
+  GQA_ERR_ALIGN = 3,       /* a pointer is not 16-byte aligned                    */
+  GQA_ERR_WORKSPACE = 4,   /* workspace missing or smaller than required          */
+  GQA_ERR_CACHE_FULL = 5,  /* (device) appended rows did not fit; they were dropped */
+  GQA_ERR_CUDA = 6,        /* a CUDA runtime call or a launch failed              */
+  GQA_ERR_TIMEOUT = 7,     /* (device) a bounded wait inside a kernel ran out     */
+  GQA_ERR_BAD_LENGTH = 8   /* (device) a seq_lens entry was negative or > S_max   */
+} gqa_status_t;
+
+typedef enum {
+  GQA_OUT_F32 = 0,   /* output written as fp32 */
+  GQA_OUT_BF16 = 1   /* output written as bf16 (round to nearest even) */
+} gqa_out_dtype_t;
+
+/* Human-readable name of a status code (static string, never NULL). */
+const char* gqa_status_string(int status);
+
+/* Library version, encoded as major*10000 + minor*100 + patch. */
+int gqa_version(void);
+
+/*
+ * gqa_prefill_fwd -- attention over a whole sequence (prefill).
+ *
+ *   O[b,i,h,:] = sum_j softmax_j(scale * Q[b,i,h,:] . K[b,j,h/G,:]) V[b,j,h/G,:]
+ *
+ * with j over all L keys, or over j <= i when `causal` != 0 (query and key
+ * positions coincide). The K/V head of query head h is h / G, G = h_q / g;
+ * K and V are read in place, never duplicated per query head (the pages'
+ * GroupedQueryAttention code, sections 2.1 and 2.3 of the zeeklog.com page).
+ *
+ *   q      [B, L, h_q, d] bf16   (projection-output layout)
+ *   k, v   [B, L, g,   d] bf16
+ *   o      [B, L, h_q, d] fp32 or bf16 per o_dtype (written, never read)
+ *   lse    optional fp32 [B, h_q, L]: natural-log sum of exp(scale * q.k)
+ *          over the visible keys of each row (written when non-NULL)
+ *   scale  softmax scale, usually 1/sqrt(d); must be finite and > 0
+ *
+ * Returns GQA_OK once the work is queued, or an error with nothing queued.
+ */
+int gqa_prefill_fwd(const void* q, const void* k, const void* v, void* o,
+                    int o_dtype, float* lse, int B, int L, int h_q, int g, int d,
+                    float scale, int causal, int32_t* status_dev, void* stream);
+
+/*
+ * gqa_decode_workspace_bytes -- device scratch bytes gqa_decode_fwd needs for
+ * these sizes (split-KV partial outputs and their log-sum-exp values).
+ * Returns 0 for sizes gqa_decode_fwd would reject.
+ */
+size_t gqa_decode_workspace_bytes(int B, int h_q, int g, int d, int S_max);
+
+/*
+ * gqa_decode_fwd -- one new query token per sequence attends over the KV
+ * cache (the autoregressive decode step of the ijyty.com explainer,
+ * section 2.1).
+ *
+ *   O[b,h,:] = sum_{j < seq_lens[b]} softmax_j(scale * q[b,h,:] . Kc[b,h/G,j,:]) Vc[b,h/G,j,:]
+ *
+ *   q          [B, h_q, d] bf16
+ *   k_cache,
+ *   v_cache    [B, g, S_max, d] bf16; rows at or past seq_lens[b] are never
+ *              used in the result (they may hold anything, NaN included)
+ *   seq_lens   device int32 [B], each in [0, S_max]; a sequence of length 0
+ *              gives an all-zero output row and lse = -inf. Entries outside
+ *              [0, S_max] are clamped and flagged GQA_ERR_BAD_LENGTH.
+ *   o          [B, h_q, d] fp32 or bf16 per o_dtype
+ *   lse        optional fp32 [B, h_q] (natural log), may be NULL
+ *   workspace  device scratch of at least gqa_decode_workspace_bytes(...)
+ *              bytes, 16-byte aligned, owned by the caller; its contents on
+ *              entry do not matter and are garbage on exit. Calls that run
+ *              concurrently on different streams need separate workspaces.
+ */
+int gqa_decode_fwd(const void* q, const void* k_cache, const void* v_cache,
+                   const int32_t* seq_lens, void* o, int o_dtype, float* lse,
+                   int B, int h_q, int g, int d, int S_max, float scale,
+                   void* workspace, size_t workspace_bytes,
+                   int32_t* status_dev, void* stream);
+
+/*
+ * kv_cache_append -- write T new tokens per sequence behind its valid rows
+ * and advance its length (the cache concatenation along the sequence axis,
+ * ijyty.com explainer section 3.2; the cache keeps only g heads).
+ *
+ *   k_cache, v_cache  [B, g, S_max, d] bf16, updated in place
+ *   seq_lens          device int32 [B], read then set to min(len + T, S_max)
+ *   k_new, v_new      [B, T, g, d] bf16 (projection-output layout)
+ *
+ * Token t of sequence b is copied bit for bit into row seq_lens[b] + t of
+ * every K/V head. Rows that would land at or past S_max are dropped and
+ * GQA_ERR_CACHE_FULL is recorded in *status_dev (if given). Two launches are
+ * queued: the row copy, then the length update.
+ */
+int kv_cache_append(void* k_cache, void* v_cache, int32_t* seq_lens,
+                    const void* k_new, const void* v_new, int B, int g, int d,
+                    int S_max, int T, int32_t* status_dev, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* GQA_B300_H */

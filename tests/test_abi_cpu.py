@@ -1,0 +1,129 @@
+"""Host-side checks of the C interface that need no GPU.
+
+The library is loaded with ctypes, every function declared in include/gqa.h
+must be exported, and argument validation must reject bad calls with the
+documented status before any CUDA call is made (so these run on a machine
+without a device or driver).
+"""
+
+import ctypes
+import os
+import re
+
+import pytest
+
+from grouped_query_attention_10_b300 import binding
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "gqa.h")
+
+FAKE = 1 << 20        # a 16-byte-aligned non-null address; never dereferenced
+MISALIGNED = FAKE + 8
+
+
+def _declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    names = re.findall(r"^\s*(?:const\s+)?[A-Za-z_][\w\s\*]*?\b([a-z_][a-z0-9_]*)\s*\(",
+                       text, flags=re.M)
+    return sorted(set(n for n in names if n not in ("if", "defined")))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    return binding.load_library()
+
+
+def test_header_declares_the_three_entry_points():
+    names = _declared_functions()
+    for n in ("gqa_prefill_fwd", "gqa_decode_fwd", "kv_cache_append",
+              "gqa_decode_workspace_bytes", "gqa_status_string", "gqa_version"):
+        assert n in names, names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for n in _declared_functions():
+        assert hasattr(lib, n), f"{n} declared in gqa.h but not exported"
+
+
+def test_version_and_status_strings(lib):
+    assert lib.gqa_version() == 100
+    for code in range(0, 9):
+        s = binding.status_string(code)
+        assert s.startswith("GQA_")
+    assert binding.status_string(99) == "GQA_ERR_UNKNOWN"
+
+
+def _prefill(lib, q=FAKE, k=FAKE, v=FAKE, o=FAKE, o_dtype=0, lse=None, B=1, L=128, h_q=8,
+             g=2, d=64, scale=0.125, causal=1, status=None):
+    return lib.gqa_prefill_fwd(q, k, v, o, o_dtype, lse, B, L, h_q, g, d, scale, causal,
+                               status, None)
+
+
+def test_prefill_validation(lib):
+    assert _prefill(lib, q=None) == binding.GQA_ERR_NULL
+    assert _prefill(lib, o=None) == binding.GQA_ERR_NULL
+    assert _prefill(lib, B=0) == binding.GQA_ERR_SHAPE
+    assert _prefill(lib, L=0) == binding.GQA_ERR_SHAPE
+    assert _prefill(lib, h_q=8, g=3) == binding.GQA_ERR_SHAPE    # g does not divide h_q
+    assert _prefill(lib, h_q=12, g=2) == binding.GQA_ERR_SHAPE   # group size 6 not a power of 2
+    assert _prefill(lib, h_q=256, g=1) == binding.GQA_ERR_SHAPE  # group size > 128
+    assert _prefill(lib, d=96) == binding.GQA_ERR_SHAPE
+    assert _prefill(lib, o_dtype=7) == binding.GQA_ERR_SHAPE
+    assert _prefill(lib, scale=0.0) == binding.GQA_ERR_SHAPE
+    assert _prefill(lib, scale=float("nan")) == binding.GQA_ERR_SHAPE
+    assert _prefill(lib, q=MISALIGNED) == binding.GQA_ERR_ALIGN
+    assert _prefill(lib, o=MISALIGNED) == binding.GQA_ERR_ALIGN
+    assert _prefill(lib, lse=FAKE + 2) == binding.GQA_ERR_ALIGN
+
+
+def _decode(lib, q=FAKE, kc=FAKE, vc=FAKE, lens=FAKE, o=FAKE, o_dtype=0, lse=None, B=4,
+            h_q=32, g=8, d=128, S_max=1024, scale=0.088, ws=FAKE, ws_bytes=None, status=None):
+    if ws_bytes is None:
+        ws_bytes = lib.gqa_decode_workspace_bytes(B, h_q, g, d, S_max)
+    return lib.gqa_decode_fwd(q, kc, vc, lens, o, o_dtype, lse, B, h_q, g, d, S_max, scale,
+                              ws, ws_bytes, status, None)
+
+
+def test_decode_workspace_bytes(lib):
+    n = lib.gqa_decode_workspace_bytes(64, 32, 8, 128, 8192)
+    assert n > 0 and n % 4 == 0
+    assert lib.gqa_decode_workspace_bytes(64, 32, 8, 96, 8192) == 0
+    assert lib.gqa_decode_workspace_bytes(0, 32, 8, 128, 8192) == 0
+    assert lib.gqa_decode_workspace_bytes(4, 32, 3, 128, 8192) == 0
+    # the partials hold one fp32 row of d values + one log-sum-exp per split
+    assert n >= 64 * 32 * 128 * 4
+
+
+def test_decode_validation(lib):
+    assert _decode(lib, q=None) == binding.GQA_ERR_NULL
+    assert _decode(lib, lens=None) == binding.GQA_ERR_NULL
+    assert _decode(lib, B=0) == binding.GQA_ERR_SHAPE
+    assert _decode(lib, S_max=0) == binding.GQA_ERR_SHAPE
+    assert _decode(lib, g=5) == binding.GQA_ERR_SHAPE
+    assert _decode(lib, d=32) == binding.GQA_ERR_SHAPE
+    assert _decode(lib, scale=-1.0) == binding.GQA_ERR_SHAPE
+    assert _decode(lib, ws=None) == binding.GQA_ERR_WORKSPACE
+    assert _decode(lib, ws_bytes=16) == binding.GQA_ERR_WORKSPACE
+    assert _decode(lib, kc=MISALIGNED) == binding.GQA_ERR_ALIGN
+    assert _decode(lib, ws=MISALIGNED) == binding.GQA_ERR_ALIGN
+    assert _decode(lib, lens=FAKE + 2) == binding.GQA_ERR_ALIGN
+
+
+def test_append_validation(lib):
+    def app(kc=FAKE, vc=FAKE, lens=FAKE, kn=FAKE, vn=FAKE, B=2, g=2, d=64, S=16, T=1):
+        return lib.kv_cache_append(kc, vc, lens, kn, vn, B, g, d, S, T, None, None)
+    assert app(kc=None) == binding.GQA_ERR_NULL
+    assert app(lens=None) == binding.GQA_ERR_NULL
+    assert app(B=0) == binding.GQA_ERR_SHAPE
+    assert app(d=48) == binding.GQA_ERR_SHAPE
+    assert app(T=-1) == binding.GQA_ERR_SHAPE
+    assert app(kn=MISALIGNED) == binding.GQA_ERR_ALIGN
+    assert app(T=0) == binding.GQA_OK  # nothing to do, nothing queued
+
+
+def test_missing_library_fails_loudly(monkeypatch, tmp_path):
+    monkeypatch.setattr(binding, "_lib", None)
+    monkeypatch.setattr(binding, "LIB_PATH", str(tmp_path / "absent.so"))
+    with pytest.raises(ImportError):
+        binding.load_library()
