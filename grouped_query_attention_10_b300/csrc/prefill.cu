@@ -9,23 +9,36 @@
 // whole group. The score matrix never leaves the chip (the on-chip softmax
 // the ijyty.com explainer credits to FlashAttention, section 4.3).
 //
-// Work unit: one CTA per (query tile, K/V head, batch). A query tile holds
-// 128 rows = (128 / G) consecutive positions x the G query heads of one K/V
-// group, stacked position-major (the G heads of one position are contiguous
-// in the [B, L, h_q, d] input, so a single 4-D TMA box fetches the tile).
-// Every K/V tile the CTA loads therefore serves all G heads of the group.
+// Work unit: one CTA per (pair of query tiles, K/V head, batch). A query tile
+// holds 128 rows = (128 / G) consecutive positions x the G query heads of one
+// K/V group, stacked position-major (the G heads of one position are
+// contiguous in the [B, L, h_q, d] input, so one 4-D TMA box fetches a tile).
+// The two tiles cover consecutive positions and share every K/V tile the CTA
+// loads, so each K/V byte brought into shared memory serves 2 x 128 rows of
+// all G heads of the group.
 //
-// Warp roles (256 threads):
-//   warp 0      TMA producer: Q once, then K and V tiles through smem rings
-//   warp 1      TMEM allocator + single-thread tcgen05.mma issuer
-//   warps 4..7  softmax: warp w owns TMEM lanes 32*(w-4) .. +31 = tile rows
-// Per K/V tile j: S_j = Q K_j^T (M=128, N=128, K=d) into one of two TMEM
-// score buffers, so S_{j+1} is computed while the softmax works on S_j; the
-// softmax writes P_j (bf16) into a 128-byte-swizzled smem tile and the MMA
-// warp accumulates O += P_j V_j (M=128, N=d, K=128) into TMEM. The online
-// softmax keeps a running row max in log2 units and rescales O lazily: only
-// when some row's max grew by more than 2^8 (exact either way, because O and
-// the row sum always share the same reference max).
+// Warp roles (384 threads):
+//   warp 0        TMA producer: both query tiles once, then K and V tiles
+//                 through shared-memory rings
+//   warp 1        TMEM allocator + tcgen05.mma issuer (the warp walks the
+//                 schedule, one elected lane issues)
+//   warps 4..7    softmax of query tile 0 (warp w owns TMEM lanes 32*(w%4)..)
+//   warps 8..11   softmax of query tile 1
+// TMEM (512 columns): S_t = scores of tile t (128 columns), O_t = output
+// accumulator of tile t (d columns). The softmax writes P_t (bf16, two per
+// 32-bit column) over the first 64 columns of S_t and the P.V product reads
+// it from there (A operand in TMEM), so P never touches shared memory.
+//
+// MMA issue order per K/V tile j: PV_0(j), S_0(j+1), PV_1(j), S_1(j+1). One
+// thread issues every MMA, and tcgen05 MMAs from one thread execute in order,
+// so S_t(j+1) overwrites S_t/P_t only after PV_t(j) has read P_t, and the
+// commit that announces S_t(j+1) also covers PV_t(j): when the softmax sees
+// S_t(j+1), O_t is final for keys < (j+1)*128 and may be rescaled in place.
+// While the softmax of one tile runs, the tensor core works on the other.
+//
+// The online softmax keeps a running row max in log2 units and rescales O
+// lazily: only when some row's max grew by more than 2^8 (exact either way,
+// because O and the row sum always share the same reference max).
 #include <cuda_bf16.h>
 
 #include "../../include/gqa.h"
@@ -38,21 +51,81 @@ namespace {
 
 constexpr int BM = kPrefillBM;
 constexpr int BN = kPrefillBN;
-constexpr int kThreads = 256;
+constexpr int kThreads = 384;
 constexpr float kRescaleThreshold = 8.0f;  // log2 units
 
 template <int D>
 struct PrefillCfg {
-  static constexpr int KS = D == 128 ? 2 : 3;  // K ring depth
+  static constexpr int KS = D == 128 ? 2 : 4;  // K ring depth
   static constexpr int VS = KS;                 // V ring depth
-  static constexpr uint32_t kQBytes = BM * D * 2;
+  static constexpr uint32_t kQTile = BM * D * 2;
   static constexpr uint32_t kKVStage = BN * D * 2;
-  static constexpr uint32_t kPBytes = BM * BN * 2;
-  static constexpr uint32_t kOffK = kQBytes;
+  static constexpr uint32_t kOffK = 2 * kQTile;
   static constexpr uint32_t kOffV = kOffK + KS * kKVStage;
-  static constexpr uint32_t kOffP = kOffV + VS * kKVStage;
-  static constexpr uint32_t kSmem = kOffP + kPBytes + 1024;  // + alignment slack
+  static constexpr uint32_t kSmem = kOffV + VS * kKVStage + 1024;  // + alignment slack
 };
+
+// Row max of one 128-key score tile in TMEM (three-input max, four chains).
+// With MASK, columns e > nvis (relative to the tile) are ignored.
+template <bool MASK>
+__device__ __forceinline__ float tile_row_max(uint32_t t_s, int nvis) {
+  float mx4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+#pragma unroll
+  for (int h = 0; h < 2; ++h) {
+    uint32_t r[64];
+    tmem_ld32(t_s + h * 64, r);
+    tmem_ld32(t_s + h * 64 + 32, r + 32);
+    tmem_ld_wait();
+#pragma unroll
+    for (int e = 0; e < 32; ++e) {
+      float a = __uint_as_float(r[2 * e]);
+      float b = __uint_as_float(r[2 * e + 1]);
+      if (MASK) {
+        if (h * 64 + 2 * e > nvis) a = -INFINITY;
+        if (h * 64 + 2 * e + 1 > nvis) b = -INFINITY;
+      }
+      mx4[e & 3] = max3f(mx4[e & 3], a, b);
+    }
+  }
+  return max3f(mx4[0], mx4[1], fmaxf(mx4[2], mx4[3]));
+}
+
+// P = 2^(s * scale_log2 - m) for one 128-key tile, written as bf16 pairs over
+// the first 64 TMEM columns of the tile; returns the row sum of P (fp32).
+// Scale-and-shift and the running sum use packed two-lane fp32 ops.
+template <bool MASK>
+__device__ __forceinline__ float tile_exp_to_p(uint32_t t_s, int nvis, float scale_log2,
+                                               float m) {
+  const uint64_t c2 = f32x2(scale_log2, scale_log2);
+  const uint64_t nm2 = f32x2(-m, -m);
+  uint64_t sum2[2] = {0ull, 0ull};
+#pragma unroll
+  for (int h = 0; h < 2; ++h) {
+    uint32_t r[64];
+    tmem_ld32(t_s + h * 64, r);
+    tmem_ld32(t_s + h * 64 + 32, r + 32);
+    tmem_ld_wait();
+    uint32_t w[32];
+#pragma unroll
+    for (int e = 0; e < 32; ++e) {
+      float xa, xb;
+      split_f32x2(ffma_x2(u32x2(r[2 * e], r[2 * e + 1]), c2, nm2), xa, xb);
+      float pa = ex2_approx(xa);
+      float pb = ex2_approx(xb);
+      if (MASK) {
+        if (h * 64 + 2 * e > nvis) pa = 0.f;
+        if (h * 64 + 2 * e + 1 > nvis) pb = 0.f;
+      }
+      sum2[e & 1] = fadd_x2(sum2[e & 1], f32x2(pa, pb));
+      w[e] = pack_bf16x2(pa, pb);
+    }
+    tmem_st32(t_s + h * 32, w);  // P columns [32h, 32h+32) hold keys [64h, 64h+64)
+  }
+  float a0, a1, b0, b1;
+  split_f32x2(sum2[0], a0, a1);
+  split_f32x2(sum2[1], b0, b1);
+  return (a0 + a1) + (b0 + b1);
+}
 
 }  // namespace
 
@@ -60,16 +133,14 @@ template <int D, bool CAUSAL>
 __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(
     const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
     const __grid_constant__ CUtensorMap tm_v, void* __restrict__ o, int o_dtype,
-    float* __restrict__ lse, int L, int h_q, int G, int G_log2, float scale_log2, int n_qtiles,
+    float* __restrict__ lse, int L, int h_q, int G, int G_log2, float scale_log2, int n_ctiles,
     int32_t* status) {
   using C = PrefillCfg<D>;
   constexpr int KS = C::KS;
   constexpr int VS = C::VS;
-  constexpr uint32_t kTmS = 0;      // two score buffers: columns [0,128) and [128,256)
-  constexpr uint32_t kTmO = 256;    // O accumulator: columns [256, 256 + D)
   constexpr uint32_t kTmCols = 512;
   constexpr uint32_t kIdescS = idesc_bf16_f32(BM, BN, false);  // Q (K-major) x K (K-major)
-  constexpr uint32_t kIdescO = idesc_bf16_f32(BM, D, true);    // P (K-major) x V (MN-major)
+  constexpr uint32_t kIdescO = idesc_bf16_f32(BM, D, true);    // P (TMEM) x V (MN-major)
 
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -79,23 +150,25 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(
   __shared__ __align__(8) uint64_t bar_ke[KS];
   __shared__ __align__(8) uint64_t bar_vf[VS];
   __shared__ __align__(8) uint64_t bar_ve[VS];
-  __shared__ __align__(8) uint64_t bar_sf[2];     // S_j ready in TMEM buffer j&1
-  __shared__ __align__(8) uint64_t bar_sfree[2];  // softmax has read TMEM buffer
-  __shared__ __align__(8) uint64_t bar_p;         // P_j written to smem
-  __shared__ __align__(8) uint64_t bar_o;         // PV_j retired (O updated, P free)
-  __shared__ __align__(8) uint64_t bar_fin;       // every MMA retired
+  __shared__ __align__(8) uint64_t bar_s[2];  // S_t(j) in TMEM (and PV_t(j-1) retired)
+  __shared__ __align__(8) uint64_t bar_p[2];  // P_t(j) written to TMEM, O_t rescaled
+  __shared__ __align__(8) uint64_t bar_o[2];  // PV_t(j) retired
+  __shared__ __align__(8) uint64_t bar_fin;   // every MMA retired
   __shared__ uint32_t tmem_base_sh;
   __shared__ int abort_flag;
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  const int qt = CAUSAL ? (n_qtiles - 1 - static_cast<int>(blockIdx.x)) : blockIdx.x;
+  const int ct = CAUSAL ? (n_ctiles - 1 - static_cast<int>(blockIdx.x)) : blockIdx.x;
   const int kvh = blockIdx.y;
   const int b = blockIdx.z;
   const int PM = BM >> G_log2;  // positions per query tile
-  const int p0 = qt * PM;
-  const int kv_end = CAUSAL ? min(L, p0 + PM) : L;
-  const int n_kv = (kv_end + BN - 1) / BN;
+  const int p0 = ct * 2 * PM;
+  // K/V tiles each query tile needs (0 for a tile that lies wholly past L)
+  const int n_kv0 = (CAUSAL ? min(L, p0 + PM) + BN - 1 : L + BN - 1) / BN;
+  const int n_kv1 =
+      p0 + PM < L ? (CAUSAL ? min(L, p0 + 2 * PM) + BN - 1 : L + BN - 1) / BN : 0;
+  const int n_kv = max(n_kv0, n_kv1);
 
   if (threadIdx.x == 0) {
     abort_flag = 0;
@@ -108,12 +181,11 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(
       mbar_init(&bar_vf[i], 1);
       mbar_init(&bar_ve[i], 1);
     }
-    for (int i = 0; i < 2; ++i) {
-      mbar_init(&bar_sf[i], 1);
-      mbar_init(&bar_sfree[i], 128);
+    for (int t = 0; t < 2; ++t) {
+      mbar_init(&bar_s[t], 1);
+      mbar_init(&bar_p[t], 128);
+      mbar_init(&bar_o[t], 1);
     }
-    mbar_init(&bar_p, 128);
-    mbar_init(&bar_o, 1);
     mbar_init(&bar_fin, 1);
     fence_mbar_init();
   }
@@ -132,10 +204,14 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(
       prefetch_tmap(&tm_q);
       prefetch_tmap(&tm_k);
       prefetch_tmap(&tm_v);
-      mbar_arrive_expect_tx(&bar_q, C::kQBytes);
+      const int n_qt = n_kv1 > 0 ? 2 : 1;
+      mbar_arrive_expect_tx(&bar_q, n_qt * C::kQTile);
+      for (int t = 0; t < n_qt; ++t) {
 #pragma unroll
-      for (int cb = 0; cb < D / 64; ++cb)
-        tma_load_4d(smem + cb * (BM * 128), &tm_q, &bar_q, cb * 64, kvh * G, p0, b);
+        for (int cb = 0; cb < D / 64; ++cb)
+          tma_load_4d(smem + t * C::kQTile + cb * (BM * 128), &tm_q, &bar_q, cb * 64, kvh * G,
+                      p0 + t * PM, b);
+      }
       int issued_k = 0, issued_v = 0;
       bool ok = true;
       for (int j = 0; j < n_kv && ok; ++j) {
@@ -171,151 +247,138 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
-    if (lane == 0) {
-      const uint32_t sQ = smem_u32(smem);
-      const uint32_t sK = sQ + C::kOffK;
-      const uint32_t sV = sQ + C::kOffV;
-      const uint32_t sP = sQ + C::kOffP;
-      bool ok = mbar_wait(&bar_q, 0, &abort_flag);
-      for (int j = 0; ok && j <= n_kv; ++j) {
-        if (j < n_kv) {
-          const int ks = j % KS;
-          ok = mbar_wait(&bar_kf[ks], (j / KS) & 1, &abort_flag);
-          if (ok && j >= 2) ok = mbar_wait(&bar_sfree[j & 1], ((j - 2) >> 1) & 1, &abort_flag);
-          if (!ok) break;
-          tc_fence_after();
-          const uint32_t d_s = tmem + kTmS + static_cast<uint32_t>(j & 1) * BN;
+    // The whole warp walks the schedule (so it stays converged and keeps the
+    // descriptors in uniform registers); one elected lane issues the MMAs.
+    const bool leader = elect_one();
+    const uint32_t sQ = smem_u32(smem);
+    // descriptor bases; a k-step only moves the 14-bit start-address field
+    const uint64_t dq0 = smem_desc_sw128(sQ, 16, 1024);
+    const uint64_t dk0 = smem_desc_sw128(sQ + C::kOffK, 16, 1024);
+    const uint64_t dv0 = smem_desc_sw128(sQ + C::kOffV, BN * 128, 1024);
+    // byte offset (>> 4) of k-step kk inside a K-major 128-byte-swizzled tile
+    auto kmaj = [](int kk) -> uint64_t {
+      return static_cast<uint64_t>(((kk >> 2) * (BM * 128) + (kk & 3) * 32) >> 4);
+    };
+    auto issue_s = [&](int t, int ks) {
+      const uint32_t d_s = tmem + static_cast<uint32_t>(t) * BN;
+      const uint64_t aq = dq0 + ((t * C::kQTile) >> 4);
+      const uint64_t bk = dk0 + ((ks * C::kKVStage) >> 4);
 #pragma unroll
-          for (int kk = 0; kk < D / 16; ++kk) {
-            const uint64_t ad =
-                smem_desc_sw128(sQ + (kk >> 2) * (BM * 128) + (kk & 3) * 32, 16, 1024);
-            const uint64_t bd = smem_desc_sw128(
-                sK + ks * C::kKVStage + (kk >> 2) * (BN * 128) + (kk & 3) * 32, 16, 1024);
-            mma_bf16_ss(d_s, ad, bd, kIdescS, kk > 0 ? 1u : 0u);
-          }
-          mma_commit(&bar_sf[j & 1]);
-          mma_commit(&bar_ke[ks]);
-        }
-        if (j >= 1) {
-          const int i = j - 1;
-          const int vs = i % VS;
-          ok = mbar_wait(&bar_p, i & 1, &abort_flag);
-          if (ok) ok = mbar_wait(&bar_vf[vs], (i / VS) & 1, &abort_flag);
-          if (!ok) break;
-          tc_fence_after();
+      for (int kk = 0; kk < D / 16; ++kk)
+        mma_bf16_ss(d_s, aq + kmaj(kk), bk + kmaj(kk), kIdescS, kk > 0 ? 1u : 0u);
+      mma_commit(&bar_s[t]);
+    };
+    auto issue_pv = [&](int t, int vs, bool first) {
+      const uint32_t p_t = tmem + static_cast<uint32_t>(t) * BN;  // P_t over S_t
+      const uint32_t o_t = tmem + 2 * BN + static_cast<uint32_t>(t) * D;
+      // V tile [BN keys x D], D contiguous: MN-major B operand; LBO = distance
+      // between the 64-wide column blocks of D; a k-step is 16 rows of 128 B
+      const uint64_t bv = dv0 + ((vs * C::kKVStage) >> 4);
 #pragma unroll
-          for (int kk = 0; kk < BN / 16; ++kk) {
-            const uint64_t ad =
-                smem_desc_sw128(sP + (kk >> 2) * (BM * 128) + (kk & 3) * 32, 16, 1024);
-            // V tile [BN keys x D] with D contiguous: MN-major B operand;
-            // LBO = distance between 64-wide column blocks of D
-            const uint64_t bd =
-                smem_desc_sw128(sV + vs * C::kKVStage + kk * (16 * 128), BN * 128, 1024);
-            mma_bf16_ss(tmem + kTmO, ad, bd, kIdescO, (i > 0 || kk > 0) ? 1u : 0u);
-          }
-          mma_commit(&bar_o);
-          mma_commit(&bar_ve[vs]);
-        }
+      for (int kk = 0; kk < BN / 16; ++kk)
+        mma_bf16_ts(o_t, p_t + kk * 8, bv + static_cast<uint64_t>((kk * 16 * 128) >> 4),
+                    kIdescO, (!first || kk > 0) ? 1u : 0u);
+      mma_commit(&bar_o[t]);
+    };
+    auto wait_all = [&](uint64_t* bar, uint32_t parity) {
+      return __all_sync(0xffffffffu, mbar_wait(bar, parity, &abort_flag));
+    };
+
+    bool ok = wait_all(&bar_q, 0) && wait_all(&bar_kf[0], 0);
+    if (ok) {
+      tc_fence_after();
+      if (leader) {
+        issue_s(0, 0);
+        if (n_kv1 > 0) issue_s(1, 0);
+        mma_commit(&bar_ke[0]);
       }
-      // every MMA must have retired before TMEM is released
+      __syncwarp();
+    }
+    for (int j = 0; ok && j < n_kv; ++j) {
+      const int vs = j % VS;
+      const int nx = j + 1;
+      const int ks = nx % KS;
+      ok = wait_all(&bar_vf[vs], (j / VS) & 1);
+      if (ok && nx < n_kv) ok = wait_all(&bar_kf[ks], (nx / KS) & 1);
+      for (int t = 0; ok && t < 2; ++t) {
+        const int n_t = t == 0 ? n_kv0 : n_kv1;
+        if (j >= n_t) continue;
+        ok = wait_all(&bar_p[t], j & 1);
+        if (!ok) break;
+        tc_fence_after();
+        if (leader) {
+          issue_pv(t, vs, j == 0);
+          if (nx < n_t) issue_s(t, ks);
+        }
+        __syncwarp();
+      }
+      if (!ok) break;
+      if (leader) {
+        mma_commit(&bar_ve[vs]);
+        if (nx < n_kv) mma_commit(&bar_ke[ks]);
+      }
+      __syncwarp();
+    }
+    // every MMA must have retired before TMEM is released
+    if (leader) {
       mma_commit(&bar_fin);
       mbar_drain(&bar_fin, 0);
     }
+    __syncwarp();
   } else if (warp >= 4) {
     // ------------------------------------------------------------ softmax
-    const int q4 = warp - 4;
-    const int row = q4 * 32 + lane;
-    const int pos = p0 + (row >> G_log2);
+    const int t = (warp - 4) >> 2;  // query tile of this warpgroup
+    const int wq = warp & 3;        // TMEM lane quadrant
+    const int row = wq * 32 + lane;
+    const int pt = p0 + t * PM;
+    const int pos = pt + (row >> G_log2);
     const int head = kvh * G + (row & (G - 1));
-    const uint32_t t_lane = tmem + (static_cast<uint32_t>(q4 * 32) << 16);
-    uint8_t* p_row = smem + C::kOffP + row * 128;
+    const uint32_t lane_base = static_cast<uint32_t>(wq * 32) << 16;
+    const uint32_t t_s = tmem + lane_base + static_cast<uint32_t>(t) * BN;
+    const uint32_t t_o = tmem + lane_base + 2 * BN + static_cast<uint32_t>(t) * D;
+    const int n_my = t == 0 ? n_kv0 : n_kv1;
+    // last key this row may see
+    const int last_key = CAUSAL ? min(L - 1, pos) : L - 1;
     float m_run = -INFINITY;  // running max of scale*log2(e)*s, possibly stale by < 2^8
     float l_run = 0.f;
     bool ok = true;
-    for (int j = 0; j < n_kv; ++j) {
-      const int buf = j & 1;
-      ok = __all_sync(0xffffffffu, mbar_wait(&bar_sf[buf], (j >> 1) & 1, &abort_flag));
+    for (int j = 0; j < n_my; ++j) {
+      ok = __all_sync(0xffffffffu, mbar_wait(&bar_s[t], j & 1, &abort_flag));
       if (!ok) break;
       tc_fence_after();
-      uint32_t sr[BN];
-#pragma unroll
-      for (int c = 0; c < BN / 32; ++c) tmem_ld32(t_lane + kTmS + buf * BN + c * 32, sr + c * 32);
-      tmem_ld_wait();
-      tc_fence_before();
-      mbar_arrive(&bar_sfree[buf]);
-      float s[BN];
-#pragma unroll
-      for (int e = 0; e < BN; ++e) s[e] = __uint_as_float(sr[e]);
-
       const int key0 = j * BN;
-      const bool need_mask = (key0 + BN > L) || (CAUSAL && key0 + BN - 1 > p0);
-      float mx = -INFINITY;
-      if (need_mask) {
-#pragma unroll
-        for (int e = 0; e < BN; ++e) {
-          const int key = key0 + e;
-          const bool vis = key < L && (!CAUSAL || key <= pos);
-          s[e] = vis ? s[e] : -INFINITY;
-          mx = fmaxf(mx, s[e]);
-        }
-      } else {
-#pragma unroll
-        for (int e = 0; e < BN; ++e) mx = fmaxf(mx, s[e]);
-      }
+      const bool need_mask = (key0 + BN > L) || (CAUSAL && key0 + BN - 1 > pt);
+      const int nvis = last_key - key0;  // tile columns e <= nvis are visible
+      const float mx = need_mask ? tile_row_max<true>(t_s, nvis) : tile_row_max<false>(t_s, nvis);
       const float m_new = fmaxf(m_run, mx * scale_log2);
-      bool waited_o = false;
       if (__any_sync(0xffffffffu, m_new > m_run + kRescaleThreshold)) {
         // the whole warp adopts its new maxima (tcgen05.ld/st are warp-wide)
-        const float alpha = (m_run == -INFINITY || m_new == -INFINITY)
-                                ? (m_run == -INFINITY ? 0.f : 1.f)
-                                : ex2_approx(m_run - m_new);
+        const float alpha = m_run == -INFINITY ? 0.f : ex2_approx(m_run - m_new);
         if (j > 0) {
-          ok = __all_sync(0xffffffffu, mbar_wait(&bar_o, (j - 1) & 1, &abort_flag));
-          if (!ok) break;
-          waited_o = true;
-          tc_fence_after();
+          // O_t holds keys < j*128 and no MMA writes it until P_t(j) is ready
 #pragma unroll
           for (int c = 0; c < D / 32; ++c) {
             uint32_t r[32];
-            tmem_ld32(t_lane + kTmO + c * 32, r);
+            tmem_ld32(t_o + c * 32, r);
             tmem_ld_wait();
 #pragma unroll
             for (int e = 0; e < 32; ++e) r[e] = __float_as_uint(__uint_as_float(r[e]) * alpha);
-            tmem_st32(t_lane + kTmO + c * 32, r);
+            tmem_st32(t_o + c * 32, r);
           }
-          tmem_st_wait();
         }
         l_run *= alpha;
         m_run = m_new;
       }
-      // P = 2^(s * scale * log2(e) - m_run), packed to bf16 pairs
-      uint32_t pk[BN / 2];
-      float rsum = 0.f;
-#pragma unroll
-      for (int e = 0; e < BN / 2; ++e) {
-        const float pa = ex2_approx(fmaf(s[2 * e], scale_log2, -m_run));
-        const float pb = ex2_approx(fmaf(s[2 * e + 1], scale_log2, -m_run));
-        rsum += pa + pb;
-        pk[e] = pack_bf16x2(pa, pb);
-      }
-      l_run += rsum;
-      if (j > 0 && !waited_o) {
-        // P_{j-1} is still being read by PV_{j-1}
-        ok = __all_sync(0xffffffffu, mbar_wait(&bar_o, (j - 1) & 1, &abort_flag));
-        if (!ok) break;
-      }
-#pragma unroll
-      for (int c = 0; c < BN / 8; ++c) {
-        const int phys = (c & 7) ^ (row & 7);
-        *reinterpret_cast<uint4*>(p_row + (c >> 3) * (BM * 128) + phys * 16) =
-            make_uint4(pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]);
-      }
-      fence_proxy_async_smem();  // generic-proxy P writes -> tensor-core reads
+      // P = 2^(s * scale * log2(e) - m_run) as bf16 pairs over S_t
+      l_run += need_mask ? tile_exp_to_p<true>(t_s, nvis, scale_log2, m_run)
+                         : tile_exp_to_p<false>(t_s, nvis, scale_log2, m_run);
+      tmem_st_wait();
       tc_fence_before();
-      mbar_arrive(&bar_p);
+      mbar_arrive(&bar_p[t]);
     }
-    if (ok) ok = __all_sync(0xffffffffu, mbar_wait(&bar_o, (n_kv - 1) & 1, &abort_flag));
-    if (ok) {
+    if (ok && n_my > 0)
+      ok = __all_sync(0xffffffffu, mbar_wait(&bar_o[t], (n_my - 1) & 1, &abort_flag));
+    if (ok && n_my > 0) {
       tc_fence_after();
       const bool store = pos < L;
       const float inv_l = 1.f / l_run;
@@ -323,7 +386,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(
 #pragma unroll
       for (int c = 0; c < D / 32; ++c) {
         uint32_t r[32];
-        tmem_ld32(t_lane + kTmO + c * 32, r);
+        tmem_ld32(t_o + c * 32, r);
         tmem_ld_wait();
         if (store) {
           if (o_dtype == GQA_OUT_F32) {
@@ -339,15 +402,15 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(
                 reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(o) + orow * D + c * 32);
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
-              uint32_t w[4];
+              uint32_t wv[4];
 #pragma unroll
-              for (int t = 0; t < 4; ++t) {
-                const float lo = __uint_as_float(r[8 * e + 2 * t]) * inv_l;
-                const float hi = __uint_as_float(r[8 * e + 2 * t + 1]) * inv_l;
+              for (int q = 0; q < 4; ++q) {
+                const float lo = __uint_as_float(r[8 * e + 2 * q]) * inv_l;
+                const float hi = __uint_as_float(r[8 * e + 2 * q + 1]) * inv_l;
                 __nv_bfloat162 v2 = __floats2bfloat162_rn(lo, hi);
-                w[t] = *reinterpret_cast<uint32_t*>(&v2);
+                wv[q] = *reinterpret_cast<uint32_t*>(&v2);
               }
-              dst[e] = make_uint4(w[0], w[1], w[2], w[3]);
+              dst[e] = make_uint4(wv[0], wv[1], wv[2], wv[3]);
             }
           }
         }
@@ -379,11 +442,11 @@ static cudaError_t launch_prefill_t(const PrefillArgs& a, cudaStream_t s) {
     attr_set = true;
   }
   const int PM = BM / a.G;
-  const int n_qtiles = (a.L + PM - 1) / PM;
-  dim3 grid(n_qtiles, a.g, a.B);
+  const int n_ctiles = (a.L + 2 * PM - 1) / (2 * PM);
+  dim3 grid(n_ctiles, a.g, a.B);
   prefill_kernel<D, CAUSAL><<<grid, kThreads, kSmem, s>>>(
       a.tm_q, a.tm_k, a.tm_v, a.o, a.o_dtype, a.lse, a.L, a.h_q, a.G, a.G_log2, a.scale_log2,
-      n_qtiles, a.status);
+      n_ctiles, a.status);
   return cudaGetLastError();
 }
 
