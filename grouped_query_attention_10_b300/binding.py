@@ -27,6 +27,7 @@ GQA_ERR_CACHE_FULL = 5
 GQA_ERR_CUDA = 6
 GQA_ERR_TIMEOUT = 7
 GQA_ERR_BAD_LENGTH = 8
+GQA_ERR_SCRATCH_LIMIT = 9
 GQA_OUT_F32 = 0
 GQA_OUT_BF16 = 1
 
@@ -64,6 +65,11 @@ def load_library() -> ctypes.CDLL:
     lib.gqa_decode_fwd.restype = i32
     lib.kv_cache_append.argtypes = [vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, vp, vp]
     lib.kv_cache_append.restype = i32
+    lib.gqa_decode_fwd_noalloc.argtypes = [vp, vp, vp, vp, vp, i32, vp, i32, i32, i32, i32, i32,
+                                           f32, vp, vp]
+    lib.gqa_decode_fwd_noalloc.restype = i32
+    lib.gqa_decode_noalloc_scratch_bytes.argtypes = []
+    lib.gqa_decode_noalloc_scratch_bytes.restype = sz
     _lib = lib
     return lib
 
@@ -171,6 +177,35 @@ def gqa_decode_fwd(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor
                             _stream_ptr(stream, q.device))
     if rc != GQA_OK:
         raise GQAError(rc, "gqa_decode_fwd")
+    return out
+
+
+def gqa_decode_fwd_noalloc(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor,
+                           seq_lens: torch.Tensor, *, out: torch.Tensor,
+                           scale: Optional[float] = None, lse: Optional[torch.Tensor] = None,
+                           status: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
+    """Decode without a workspace: the library's built-in scratch array holds
+    the split partials. ``out`` must be given (this call allocates nothing)."""
+    lib = load_library()
+    B, h_q, d = q.shape
+    g, S_max = k_cache.shape[1], k_cache.shape[2]
+    _check(q, "q", torch.bfloat16)
+    _check(k_cache, "k_cache", torch.bfloat16, (B, g, S_max, d))
+    _check(v_cache, "v_cache", torch.bfloat16, (B, g, S_max, d))
+    _check(seq_lens, "seq_lens", torch.int32, (B,))
+    _check(out, "out", out.dtype, (B, h_q, d))
+    if lse is not None:
+        _check(lse, "lse", torch.float32, (B, h_q))
+    if status is not None:
+        _check(status, "status", torch.int32)
+    if scale is None:
+        scale = 1.0 / (d ** 0.5)
+    rc = lib.gqa_decode_fwd_noalloc(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(seq_lens),
+                                    _ptr(out), _out_code(out.dtype), _ptr(lse), B, h_q, g, d,
+                                    S_max, float(scale), _ptr(status),
+                                    _stream_ptr(stream, q.device))
+    if rc != GQA_OK:
+        raise GQAError(rc, "gqa_decode_fwd_noalloc")
     return out
 
 

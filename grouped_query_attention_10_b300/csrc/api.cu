@@ -106,6 +106,8 @@ const char* gqa_status_string(int status) {
     case GQA_ERR_CUDA: return "GQA_ERR_CUDA: a CUDA call or launch failed";
     case GQA_ERR_TIMEOUT: return "GQA_ERR_TIMEOUT: a bounded wait inside a kernel ran out";
     case GQA_ERR_BAD_LENGTH: return "GQA_ERR_BAD_LENGTH: a sequence length was out of range";
+    case GQA_ERR_SCRATCH_LIMIT:
+      return "GQA_ERR_SCRATCH_LIMIT: sizes need more than the built-in decode scratch";
     default: return "GQA_ERR_UNKNOWN";
   }
 }

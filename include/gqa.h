@@ -50,7 +50,8 @@ typedef enum {
   GQA_ERR_CACHE_FULL = 5,  /* (device) appended rows did not fit; they were dropped */
   GQA_ERR_CUDA = 6,        /* a CUDA runtime call or a launch failed              */
   GQA_ERR_TIMEOUT = 7,     /* (device) a bounded wait inside a kernel ran out     */
-  GQA_ERR_BAD_LENGTH = 8   /* (device) a seq_lens entry was negative or > S_max   */
+  GQA_ERR_BAD_LENGTH = 8,  /* (device) a seq_lens entry was negative or > S_max   */
+  GQA_ERR_SCRATCH_LIMIT = 9 /* the sizes need more scratch than the built-in array */
 } gqa_status_t;
 
 typedef enum {
@@ -138,6 +139,39 @@ int gqa_decode_fwd(const void* q, const void* k_cache, const void* v_cache,
 int kv_cache_append(void* k_cache, void* v_cache, int32_t* seq_lens,
                     const void* k_new, const void* v_new, int B, int g, int d,
                     int S_max, int T, int32_t* status_dev, void* stream);
+
+/*
+ * gqa_decode_fwd_noalloc -- gqa_decode_fwd for callers that cannot allocate.
+ * The pages have no counterpart of this entry point; it exists for callers
+ * that cannot hand over a workspace: plugin hosts that pass a library only
+ * its inputs and outputs while their memory planner owns every other
+ * allocation, and serving loops that must not call cudaMalloc after start-up
+ * because it can synchronise the device.
+ *
+ * Same arguments, layouts and results as gqa_decode_fwd, minus the
+ * workspace: the split-KV partials go to a scratch array built into the
+ * library (gqa_decode_noalloc_scratch_bytes() bytes, 16 MiB), which every GPU
+ * that loads the library holds until the process exits. The call allocates
+ * nothing. Sizes whose gqa_decode_workspace_bytes exceeds the array are
+ * rejected with GQA_ERR_SCRATCH_LIMIT before anything is queued (for
+ * d = 128, h_q = 32, g = 8 the ragged B = 64, S_max = 8192 cache needs about
+ * 8 MiB).
+ *
+ *  - The first call made while a device is current looks up the array's
+ *    device address on that device (cudaGetSymbolAddress) and keeps it; make
+ *    that first call before any stream capture on that device.
+ *  - Every call shares the one array per device. Nothing in it has to start
+ *    at zero (each call writes the partials it reads), but calls that overlap
+ *    on the GPU (different streams, or different host threads) race on it
+ *    and give wrong results; serialise them.
+ */
+int gqa_decode_fwd_noalloc(const void* q, const void* k_cache, const void* v_cache,
+                           const int32_t* seq_lens, void* o, int o_dtype, float* lse, int B,
+                           int h_q, int g, int d, int S_max, float scale, int32_t* status_dev,
+                           void* stream);
+
+/* Size in bytes of the scratch array behind gqa_decode_fwd_noalloc. */
+size_t gqa_decode_noalloc_scratch_bytes(void);
 
 #ifdef __cplusplus
 }
