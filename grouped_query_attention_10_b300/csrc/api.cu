@@ -33,17 +33,22 @@ EncodeTiledFn encode_fn() {
   return fn;
 }
 
-// bf16 tensor map with the 128-byte swizzle; dims/strides innermost first,
-// strides in bytes for dims 1..rank-1. Out-of-range boxes read zeros.
-bool encode_bf16(CUtensorMap* m, int rank, const void* base, const cuuint64_t* dims,
-                 const cuuint64_t* strides, const cuuint32_t* box) {
+// Tensor map with the 128-byte swizzle; dims/strides innermost first,
+// strides in bytes for dims 1..rank-1. Out-of-range boxes read zeros (loads)
+// or are skipped (stores).
+bool encode_sw128(CUtensorMap* m, CUtensorMapDataType dt, int rank, const void* base,
+                  const cuuint64_t* dims, const cuuint64_t* strides, const cuuint32_t* box) {
   EncodeTiledFn fn = encode_fn();
   if (fn == nullptr) return false;
   const cuuint32_t es[5] = {1, 1, 1, 1, 1};
-  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, static_cast<cuuint32_t>(rank),
-            const_cast<void*>(base), dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
-            CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+  return fn(m, dt, static_cast<cuuint32_t>(rank), const_cast<void*>(base), dims, strides, box,
+            es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+bool encode_bf16(CUtensorMap* m, int rank, const void* base, const cuuint64_t* dims,
+                 const cuuint64_t* strides, const cuuint32_t* box) {
+  return encode_sw128(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, rank, base, dims, strides, box);
 }
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
@@ -122,6 +127,11 @@ int gqa_prefill_fwd(const void* q, const void* k, const void* v, void* o, int o_
   if (o_dtype != GQA_OUT_F32 && o_dtype != GQA_OUT_BF16) return GQA_ERR_SHAPE;
   if (!scale_ok(scale)) return GQA_ERR_SHAPE;
   if (static_cast<long long>(B) * L * h_q * d >= kMaxElems) return GQA_ERR_SHAPE;
+  {
+    // work units (pairs of 128-row query tiles x K/V heads x batch) index an int
+    const long long pm2 = 2LL * (gqa::kPrefillBM / (h_q / g));
+    if ((L + pm2 - 1) / pm2 * g * B >= (1LL << 31)) return GQA_ERR_SHAPE;
+  }
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o)) return GQA_ERR_ALIGN;
   if (lse != nullptr && !aligned4(lse)) return GQA_ERR_ALIGN;
   if (status_dev != nullptr && !aligned4(status_dev)) return GQA_ERR_ALIGN;
@@ -137,6 +147,16 @@ int gqa_prefill_fwd(const void* q, const void* k, const void* v, void* o, int o_
     const cuuint32_t box[4] = {64, static_cast<cuuint32_t>(G),
                                static_cast<cuuint32_t>(gqa::kPrefillBM / G), 1};
     if (!encode_bf16(&a.tm_q, 4, q, dims, strides, box)) return GQA_ERR_CUDA;
+    // the output has the query layout; boxes are 128-byte column chunks
+    const cuuint64_t oe = o_dtype == GQA_OUT_F32 ? 4 : 2;
+    const cuuint64_t ostrides[3] = {d * oe, static_cast<cuuint64_t>(h_q) * d * oe,
+                                    static_cast<cuuint64_t>(L) * h_q * d * oe};
+    const cuuint32_t obox[4] = {static_cast<cuuint32_t>(128 / oe), static_cast<cuuint32_t>(G),
+                                static_cast<cuuint32_t>(gqa::kPrefillBM / G), 1};
+    if (!encode_sw128(&a.tm_o, o_dtype == GQA_OUT_F32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32
+                                                      : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,
+                      4, o, dims, ostrides, obox))
+      return GQA_ERR_CUDA;
   }
   {
     const cuuint64_t dims[4] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(g),

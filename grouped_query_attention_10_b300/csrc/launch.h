@@ -18,6 +18,7 @@ constexpr int kDecodeStage = 64;
 
 struct PrefillArgs {
   CUtensorMap tm_q, tm_k, tm_v;
+  CUtensorMap tm_o;  // output, 128-byte-wide column chunks (32 fp32 or 64 bf16)
   void* o;
   int o_dtype;
   float* lse;

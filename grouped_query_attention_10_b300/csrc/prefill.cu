@@ -9,31 +9,38 @@
 // whole group. The score matrix never leaves the chip (the on-chip softmax
 // the ijyty.com explainer credits to FlashAttention, section 4.3).
 //
-// Work unit: one CTA per (pair of query tiles, K/V head, batch). A query tile
-// holds 128 rows = (128 / G) consecutive positions x the G query heads of one
-// K/V group, stacked position-major (the G heads of one position are
-// contiguous in the [B, L, h_q, d] input, so one 4-D TMA box fetches a tile).
-// The two tiles cover consecutive positions and share every K/V tile the CTA
-// loads, so each K/V byte brought into shared memory serves 2 x 128 rows of
-// all G heads of the group.
+// Work unit: (pair of query tiles, K/V head, batch). A query tile holds 128
+// rows = (128 / G) consecutive positions x the G query heads of one K/V
+// group, stacked position-major (the G heads of one position are contiguous
+// in the [B, L, h_q, d] input, so one 4-D TMA box fetches a tile). The two
+// tiles cover consecutive positions and share every K/V tile the CTA loads,
+// so each K/V byte brought into shared memory serves 2 x 128 rows of all G
+// heads of the group.
+//
+// The kernel is persistent: one CTA per SM walks the units u = blockIdx.x,
+// blockIdx.x + gridDim.x, ... (causal units ordered longest first). The K/V
+// rings, the barrier phases and the TMEM buffers carry over from one unit to
+// the next, so the loads and score products of the next unit overlap the
+// output epilogue of the current one.
 //
 // Warp roles (384 threads):
-//   warp 0        TMA producer: both query tiles once, then K and V tiles
-//                 through shared-memory rings
-//   warp 1        TMEM allocator + tcgen05.mma issuer (the warp walks the
-//                 schedule, one elected lane issues)
-//   warps 4..7    softmax of query tile 0 (warp w owns TMEM lanes 32*(w%4)..)
-//   warps 8..11   softmax of query tile 1
+//   warp 0        TMA producer: query tiles, then K and V tiles through
+//                 shared-memory rings
+//   warp 1        TMEM allocator + tcgen05.mma issuer of query tile 0
+//   warp 2        tcgen05.mma issuer of query tile 1 (each issuer warp walks
+//                 the schedule, one elected lane issues)
+//   warps 4..7    softmax + epilogue of query tile 0 (warp w owns TMEM lanes
+//                 32*(w%4)..)
+//   warps 8..11   softmax + epilogue of query tile 1
 // TMEM (512 columns): S_t = scores of tile t (128 columns), O_t = output
-// accumulator of tile t (d columns). The softmax writes P_t (bf16, two per
-// 32-bit column) over the first 64 columns of S_t and the P.V product reads
-// it from there (A operand in TMEM), so P never touches shared memory.
-//
-// MMA issue order per K/V tile j: PV_0(j), S_0(j+1), PV_1(j), S_1(j+1). One
-// thread issues every MMA, and tcgen05 MMAs from one thread execute in order,
-// so S_t(j+1) overwrites S_t/P_t only after PV_t(j) has read P_t, and the
-// commit that announces S_t(j+1) also covers PV_t(j): when the softmax sees
-// S_t(j+1), O_t is final for keys < (j+1)*128 and may be rescaled in place.
+// accumulator of tile t (d columns), P_t = probabilities (bf16, two per
+// 32-bit column, 64 columns) read by the P.V product as the A operand.
+//  * d = 64: P_t has columns of its own. The softmax releases S_t as soon as
+//    it has read the scores into registers, so S_t(j+1) = Q K_{j+1}^T runs on
+//    the tensor core while the exponentials of tile j are computed.
+//  * d = 128: S and O fill TMEM, so P_t overwrites the first 64 columns of
+//    S_t and S_t(j+1) is issued after P_t(j).V_j (one thread issues all of
+//    tile t's MMAs, and tcgen05 MMAs from one thread execute in order).
 // While the softmax of one tile runs, the tensor core works on the other.
 //
 // The online softmax keeps a running row max in log2 units and rescales O
@@ -54,77 +61,87 @@ constexpr int BN = kPrefillBN;
 constexpr int kThreads = 384;
 constexpr float kRescaleThreshold = 8.0f;  // log2 units
 
+// Register plan. The kernel is built for 168 registers per thread (the most
+// 384 threads may hold on one SM); right after set-up the control warpgroup
+// (producer, two MMA issuers, one idle warp) gives registers back and the two
+// softmax warpgroups take them, so a softmax thread can hold a whole
+// 128-column score row. The launcher refuses to launch unless the built
+// kernel uses exactly kRegsLaunch registers, so the increase always finds
+// the registers the decrease released.
+constexpr int kRegsLaunch = 168;
+constexpr int kRegsCtl = 80;
+constexpr int kRegsSoftmax = 208;
+static_assert(128 * kRegsCtl + 256 * kRegsSoftmax <= kThreads * kRegsLaunch,
+              "register plan exceeds the launch pool");
+static_assert(kThreads * kRegsLaunch <= 65536, "launch pool exceeds the register file");
+
 template <int D>
 struct PrefillCfg {
-  static constexpr int KS = D == 128 ? 2 : 4;  // K ring depth
-  static constexpr int VS = KS;                 // V ring depth
-  static constexpr uint32_t kQTile = BM * D * 2;
+  static constexpr bool kSepP = D == 64;           // P_t has TMEM columns of its own
+  static constexpr int NQ = D == 64 ? 2 : 1;       // query-tile buffers (units in flight)
+  static constexpr int KS = D == 128 ? 2 : 3;      // K ring depth
+  static constexpr int VS = KS;                    // V ring depth
+  static constexpr uint32_t kQTile = BM * D * 2;   // one 128-row query tile
+  static constexpr uint32_t kQSlot = 2 * kQTile;   // both query tiles of a unit
   static constexpr uint32_t kKVStage = BN * D * 2;
-  static constexpr uint32_t kOffK = 2 * kQTile;
+  static constexpr uint32_t kOffK = NQ * kQSlot;
   static constexpr uint32_t kOffV = kOffK + KS * kKVStage;
-  static constexpr uint32_t kSmem = kOffV + VS * kKVStage + 1024;  // + alignment slack
+  // Output staging, per query tile: 128 rows x kStageChunks 128-byte column
+  // chunks (a chunk = 32 fp32 or 64 bf16 columns), written by the softmax
+  // threads and stored by TMA (d = 64: the whole tile in one pass).
+  static constexpr int kStageChunks = D == 64 ? 2 : 1;
+  static constexpr uint32_t kChunkBytes = BM * 128;
+  static constexpr uint32_t kStageBytes = kStageChunks * kChunkBytes;
+  static constexpr uint32_t kOffStage = kOffV + VS * kKVStage;
+  static constexpr uint32_t kSmem = kOffStage + 2 * kStageBytes + 1024;  // + alignment slack
+  // TMEM columns
+  static constexpr uint32_t kColO = 2 * BN;                   // O_t at kColO + t * D
+  static constexpr uint32_t kColP = kSepP ? 2 * BN + 2 * D : 0;
+  static constexpr uint32_t kStrideP = kSepP ? BN / 2 : BN;   // P_t at kColP + t * kStrideP
 };
 
-// Row max of one 128-key score tile in TMEM (three-input max, four chains).
-// With MASK, columns e > nvis (relative to the tile) are ignored.
-template <bool MASK>
-__device__ __forceinline__ float tile_row_max(uint32_t t_s, int nvis) {
-  float mx4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
-#pragma unroll
-  for (int h = 0; h < 2; ++h) {
-    uint32_t r[64];
-    tmem_ld32(t_s + h * 64, r);
-    tmem_ld32(t_s + h * 64 + 32, r + 32);
-    tmem_ld_wait();
-#pragma unroll
-    for (int e = 0; e < 32; ++e) {
-      float a = __uint_as_float(r[2 * e]);
-      float b = __uint_as_float(r[2 * e + 1]);
-      if (MASK) {
-        if (h * 64 + 2 * e > nvis) a = -INFINITY;
-        if (h * 64 + 2 * e + 1 > nvis) b = -INFINITY;
-      }
-      mx4[e & 3] = max3f(mx4[e & 3], a, b);
-    }
+// One decoded work unit.
+struct Unit {
+  int b, kvh, p0;  // batch, K/V head, first position of query tile 0
+  int n0, n1;      // K/V tiles seen by query tile 0 / 1 (n1 = 0: tile 1 lies past L)
+};
+
+__device__ __forceinline__ Unit decode_unit(int u, int n_ctiles, int g, int L, int PM,
+                                            bool causal, int n_pairs, int n_units) {
+  int ct, pair;
+  if (causal) {
+    // longest units first (later query tiles see more keys), dealt to the
+    // CTAs in snake order (every other round reversed) so that each CTA's
+    // total work comes out nearly equal
+    const int G0 = static_cast<int>(gridDim.x);
+    const int round = u / G0;
+    const bool flip = (round & 1) && (round + 1) * G0 <= n_units;  // full rounds only
+    const int r = flip ? round * G0 + (G0 - 1 - u % G0) : u;
+    ct = n_ctiles - 1 - r / n_pairs;
+    pair = r % n_pairs;
+  } else {
+    // consecutive units share the (batch, K/V head), so CTAs that run at the
+    // same time read the same K/V tiles and hit in L2
+    ct = u % n_ctiles;
+    pair = u / n_ctiles;
   }
-  return max3f(mx4[0], mx4[1], fmaxf(mx4[2], mx4[3]));
+  Unit w;
+  w.kvh = pair % g;
+  w.b = pair / g;
+  w.p0 = ct * 2 * PM;
+  const int all = (L + BN - 1) / BN;
+  w.n0 = causal ? (min(L, w.p0 + PM) + BN - 1) / BN : all;
+  w.n1 = w.p0 + PM < L ? (causal ? (min(L, w.p0 + 2 * PM) + BN - 1) / BN : all) : 0;
+  return w;
 }
 
-// P = 2^(s * scale_log2 - m) for one 128-key tile, written as bf16 pairs over
-// the first 64 TMEM columns of the tile; returns the row sum of P (fp32).
-// Scale-and-shift and the running sum use packed two-lane fp32 ops.
-template <bool MASK>
-__device__ __forceinline__ float tile_exp_to_p(uint32_t t_s, int nvis, float scale_log2,
-                                               float m) {
-  const uint64_t c2 = f32x2(scale_log2, scale_log2);
-  const uint64_t nm2 = f32x2(-m, -m);
-  uint64_t sum2[2] = {0ull, 0ull};
-#pragma unroll
-  for (int h = 0; h < 2; ++h) {
-    uint32_t r[64];
-    tmem_ld32(t_s + h * 64, r);
-    tmem_ld32(t_s + h * 64 + 32, r + 32);
-    tmem_ld_wait();
-    uint32_t w[32];
-#pragma unroll
-    for (int e = 0; e < 32; ++e) {
-      float xa, xb;
-      split_f32x2(ffma_x2(u32x2(r[2 * e], r[2 * e + 1]), c2, nm2), xa, xb);
-      float pa = ex2_approx(xa);
-      float pb = ex2_approx(xb);
-      if (MASK) {
-        if (h * 64 + 2 * e > nvis) pa = 0.f;
-        if (h * 64 + 2 * e + 1 > nvis) pb = 0.f;
-      }
-      sum2[e & 1] = fadd_x2(sum2[e & 1], f32x2(pa, pb));
-      w[e] = pack_bf16x2(pa, pb);
-    }
-    tmem_st32(t_s + h * 32, w);  // P columns [32h, 32h+32) hold keys [64h, 64h+64)
+// Drain helper for the abort path: wait (bounded) for the last fill issued
+// into every slot of a ring whose fills were numbered 0 .. issued-1.
+__device__ __forceinline__ void drain_ring(uint64_t* full, int depth, int issued) {
+  for (int s = 0; s < depth && s < issued; ++s) {
+    const int last = s + ((issued - 1 - s) / depth) * depth;
+    mbar_drain(&full[s], (last / depth) & 1);
   }
-  float a0, a1, b0, b1;
-  split_f32x2(sum2[0], a0, a1);
-  split_f32x2(sum2[1], b0, b1);
-  return (a0 + a1) + (b0 + b1);
 }
 
 }  // namespace
@@ -132,12 +149,14 @@ __device__ __forceinline__ float tile_exp_to_p(uint32_t t_s, int nvis, float sca
 template <int D, bool CAUSAL>
 __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(
     const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
-    const __grid_constant__ CUtensorMap tm_v, void* __restrict__ o, int o_dtype,
-    float* __restrict__ lse, int L, int h_q, int G, int G_log2, float scale_log2, int n_ctiles,
-    int32_t* status) {
+    const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_o,
+    int o_dtype, float* __restrict__ lse, int B, int L, int h_q, int g, int G, int G_log2, float scale_log2,
+    int n_ctiles, int n_units, int32_t* status) {
   using C = PrefillCfg<D>;
   constexpr int KS = C::KS;
   constexpr int VS = C::VS;
+  constexpr int NQ = C::NQ;
+  constexpr bool kSepP = C::kSepP;
   constexpr uint32_t kTmCols = 512;
   constexpr uint32_t kIdescS = idesc_bf16_f32(BM, BN, false);  // Q (K-major) x K (K-major)
   constexpr uint32_t kIdescO = idesc_bf16_f32(BM, D, true);    // P (TMEM) x V (MN-major)
@@ -145,48 +164,56 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
-  __shared__ __align__(8) uint64_t bar_q;
+  __shared__ __align__(8) uint64_t bar_q[NQ];   // query tiles landed
+  __shared__ __align__(8) uint64_t bar_qe[NQ];  // every S MMA of the unit retired
   __shared__ __align__(8) uint64_t bar_kf[KS];
   __shared__ __align__(8) uint64_t bar_ke[KS];
   __shared__ __align__(8) uint64_t bar_vf[VS];
   __shared__ __align__(8) uint64_t bar_ve[VS];
-  __shared__ __align__(8) uint64_t bar_s[2];  // S_t(j) in TMEM (and PV_t(j-1) retired)
-  __shared__ __align__(8) uint64_t bar_p[2];  // P_t(j) written to TMEM, O_t rescaled
-  __shared__ __align__(8) uint64_t bar_o[2];  // PV_t(j) retired
-  __shared__ __align__(8) uint64_t bar_fin;   // every MMA retired
+  __shared__ __align__(8) uint64_t bar_s[2];    // S_t in TMEM
+  __shared__ __align__(8) uint64_t bar_sf[2];   // S_t read by the softmax (separate-P only)
+  __shared__ __align__(8) uint64_t bar_p[2];    // P_t written to TMEM (and O_t rescaled)
+  __shared__ __align__(8) uint64_t bar_o[2];    // P_t.V retired
+  __shared__ __align__(8) uint64_t bar_fin[2];  // every MMA of issuer t retired
+  __shared__ __align__(8) uint64_t bar_stw[2];  // output stage t written (128 arrivals)
+  __shared__ __align__(8) uint64_t bar_stf[2];  // output stage t free again
+  __shared__ __align__(8) uint64_t bar_turn[4]; // exponential phases, one per SM sub-partition
   __shared__ uint32_t tmem_base_sh;
   __shared__ int abort_flag;
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  const int ct = CAUSAL ? (n_ctiles - 1 - static_cast<int>(blockIdx.x)) : blockIdx.x;
-  const int kvh = blockIdx.y;
-  const int b = blockIdx.z;
   const int PM = BM >> G_log2;  // positions per query tile
-  const int p0 = ct * 2 * PM;
-  // K/V tiles each query tile needs (0 for a tile that lies wholly past L)
-  const int n_kv0 = (CAUSAL ? min(L, p0 + PM) + BN - 1 : L + BN - 1) / BN;
-  const int n_kv1 =
-      p0 + PM < L ? (CAUSAL ? min(L, p0 + 2 * PM) + BN - 1 : L + BN - 1) / BN : 0;
-  const int n_kv = max(n_kv0, n_kv1);
+  const int n_pairs = g * B;    // (batch, K/V head) pairs
 
   if (threadIdx.x == 0) {
     abort_flag = 0;
-    mbar_init(&bar_q, 1);
+    // empty barriers take one arrival from each of the two MMA issuers
+    for (int i = 0; i < NQ; ++i) {
+      mbar_init(&bar_q[i], 1);
+      mbar_init(&bar_qe[i], 2);
+    }
     for (int i = 0; i < KS; ++i) {
       mbar_init(&bar_kf[i], 1);
-      mbar_init(&bar_ke[i], 1);
+      mbar_init(&bar_ke[i], 2);
     }
     for (int i = 0; i < VS; ++i) {
       mbar_init(&bar_vf[i], 1);
-      mbar_init(&bar_ve[i], 1);
+      mbar_init(&bar_ve[i], 2);
     }
     for (int t = 0; t < 2; ++t) {
       mbar_init(&bar_s[t], 1);
+      mbar_init(&bar_sf[t], 128);
       mbar_init(&bar_p[t], 128);
       mbar_init(&bar_o[t], 1);
     }
-    mbar_init(&bar_fin, 1);
+    mbar_init(&bar_fin[0], 1);
+    mbar_init(&bar_fin[1], 1);
+    mbar_init(&bar_stw[0], 128);
+    mbar_init(&bar_stw[1], 128);
+    mbar_init(&bar_stf[0], 1);
+    mbar_init(&bar_stf[1], 1);
+    for (int q = 0; q < 4; ++q) mbar_init(&bar_turn[q], 32);
     fence_mbar_init();
   }
   if (warp == 1) {
@@ -197,83 +224,97 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = tmem_base_sh;
-
+  if (warp < 4) {
+  setmaxnreg_dec<kRegsCtl>();
   if (warp == 0) {
     // ------------------------------------------------------------ producer
     if (lane == 0) {
       prefetch_tmap(&tm_q);
       prefetch_tmap(&tm_k);
       prefetch_tmap(&tm_v);
-      const int n_qt = n_kv1 > 0 ? 2 : 1;
-      mbar_arrive_expect_tx(&bar_q, n_qt * C::kQTile);
-      for (int t = 0; t < n_qt; ++t) {
-#pragma unroll
-        for (int cb = 0; cb < D / 64; ++cb)
-          tma_load_4d(smem + t * C::kQTile + cb * (BM * 128), &tm_q, &bar_q, cb * 64, kvh * G,
-                      p0 + t * PM, b);
-      }
-      int issued_k = 0, issued_v = 0;
+      int nu = 0, kc = 0, vc = 0;  // units, K tiles and V tiles issued so far
       bool ok = true;
-      for (int j = 0; j < n_kv && ok; ++j) {
-        const int ks = j % KS;
-        if (j >= KS) ok = mbar_wait(&bar_ke[ks], ((j / KS) - 1) & 1, &abort_flag);
+      for (int u = blockIdx.x; u < n_units && ok; u += gridDim.x, ++nu) {
+        const Unit w = decode_unit(u, n_ctiles, g, L, PM, CAUSAL, n_pairs, n_units);
+        const int n_kv = max(w.n0, w.n1);
+        const int qs = nu % NQ;
+        if (nu >= NQ) ok = mbar_wait(&bar_qe[qs], ((nu / NQ) - 1) & 1, &abort_flag);
         if (!ok) break;
-        mbar_arrive_expect_tx(&bar_kf[ks], C::kKVStage);
+        const int n_qt = w.n1 > 0 ? 2 : 1;
+        mbar_arrive_expect_tx(&bar_q[qs], n_qt * C::kQTile);
+        for (int t = 0; t < n_qt; ++t) {
 #pragma unroll
-        for (int cb = 0; cb < D / 64; ++cb)
-          tma_load_4d(smem + C::kOffK + ks * C::kKVStage + cb * (BN * 128), &tm_k, &bar_kf[ks],
-                      cb * 64, kvh, j * BN, b);
-        issued_k = j + 1;
-        const int vs = j % VS;
-        if (j >= VS) ok = mbar_wait(&bar_ve[vs], ((j / VS) - 1) & 1, &abort_flag);
-        if (!ok) break;
-        mbar_arrive_expect_tx(&bar_vf[vs], C::kKVStage);
+          for (int cb = 0; cb < D / 64; ++cb)
+            tma_load_4d(smem + qs * C::kQSlot + t * C::kQTile + cb * (BM * 128), &tm_q,
+                        &bar_q[qs], cb * 64, w.kvh * G, w.p0 + t * PM, w.b);
+        }
+        for (int j = 0; j < n_kv && ok; ++j) {
+          const int ks = kc % KS;
+          if (kc >= KS) ok = mbar_wait(&bar_ke[ks], ((kc / KS) - 1) & 1, &abort_flag);
+          if (!ok) break;
+          mbar_arrive_expect_tx(&bar_kf[ks], C::kKVStage);
 #pragma unroll
-        for (int cb = 0; cb < D / 64; ++cb)
-          tma_load_4d(smem + C::kOffV + vs * C::kKVStage + cb * (BN * 128), &tm_v, &bar_vf[vs],
-                      cb * 64, kvh, j * BN, b);
-        issued_v = j + 1;
+          for (int cb = 0; cb < D / 64; ++cb)
+            tma_load_4d(smem + C::kOffK + ks * C::kKVStage + cb * (BN * 128), &tm_k,
+                        &bar_kf[ks], cb * 64, w.kvh, j * BN, w.b);
+          ++kc;
+          const int vs = vc % VS;
+          if (vc >= VS) ok = mbar_wait(&bar_ve[vs], ((vc / VS) - 1) & 1, &abort_flag);
+          if (!ok) break;
+          mbar_arrive_expect_tx(&bar_vf[vs], C::kKVStage);
+#pragma unroll
+          for (int cb = 0; cb < D / 64; ++cb)
+            tma_load_4d(smem + C::kOffV + vs * C::kKVStage + cb * (BN * 128), &tm_v,
+                        &bar_vf[vs], cb * 64, w.kvh, j * BN, w.b);
+          ++vc;
+        }
+        if (!ok) {
+          ++nu;  // this unit's query load was issued
+          break;
+        }
       }
-      // every issued copy must have landed before the CTA may exit
-      mbar_drain(&bar_q, 0);
-      for (int s = 0; s < KS && s < issued_k; ++s) {
-        const int last = s + ((issued_k - 1 - s) / KS) * KS;
-        mbar_drain(&bar_kf[s], (last / KS) & 1);
-      }
-      for (int s = 0; s < VS && s < issued_v; ++s) {
-        const int last = s + ((issued_v - 1 - s) / VS) * VS;
-        mbar_drain(&bar_vf[s], (last / VS) & 1);
+      if (!ok) {
+        // every issued copy must have landed before the CTA may exit
+        drain_ring(bar_q, NQ, nu);
+        drain_ring(bar_kf, KS, kc);
+        drain_ring(bar_vf, VS, vc);
       }
     }
-  } else if (warp == 1) {
-    // ------------------------------------------------------------ MMA issuer
-    // The whole warp walks the schedule (so it stays converged and keeps the
-    // descriptors in uniform registers); one elected lane issues the MMAs.
+  } else if (warp <= 2) {
+    // ------------------------------------------------------------ MMA issuers
+    // Warp 1 + t issues every MMA of query tile t, so the two tiles' chains
+    // (S_t -> softmax -> P_t.V) never wait on each other's hand-offs. The
+    // whole warp walks the schedule (it stays converged and keeps the
+    // descriptors in uniform registers); one elected lane issues. A K/V ring
+    // slot (and the query slot) is released once BOTH issuers are done with
+    // it: the empty barriers count two arrivals, a commit from an issuer that
+    // used the slot or a plain arrive from one that did not.
+    const int t = warp - 1;
     const bool leader = elect_one();
-    const uint32_t sQ = smem_u32(smem);
+    const uint32_t sbase = smem_u32(smem);
     // descriptor bases; a k-step only moves the 14-bit start-address field
-    const uint64_t dq0 = smem_desc_sw128(sQ, 16, 1024);
-    const uint64_t dk0 = smem_desc_sw128(sQ + C::kOffK, 16, 1024);
-    const uint64_t dv0 = smem_desc_sw128(sQ + C::kOffV, BN * 128, 1024);
+    const uint64_t dq0 = smem_desc_sw128(sbase + t * C::kQTile, 16, 1024);
+    const uint64_t dk0 = smem_desc_sw128(sbase + C::kOffK, 16, 1024);
+    const uint64_t dv0 = smem_desc_sw128(sbase + C::kOffV, BN * 128, 1024);
+    const uint32_t d_s = tmem + static_cast<uint32_t>(t) * BN;
+    const uint32_t p_t = tmem + C::kColP + static_cast<uint32_t>(t) * C::kStrideP;
+    const uint32_t o_t = tmem + C::kColO + static_cast<uint32_t>(t) * D;
     // byte offset (>> 4) of k-step kk inside a K-major 128-byte-swizzled tile
     auto kmaj = [](int kk) -> uint64_t {
       return static_cast<uint64_t>(((kk >> 2) * (BM * 128) + (kk & 3) * 32) >> 4);
     };
-    auto issue_s = [&](int t, int ks) {
-      const uint32_t d_s = tmem + static_cast<uint32_t>(t) * BN;
-      const uint64_t aq = dq0 + ((t * C::kQTile) >> 4);
-      const uint64_t bk = dk0 + ((ks * C::kKVStage) >> 4);
+    auto issue_s = [&](int qs, int ks) {
+      const uint64_t aq = dq0 + static_cast<uint64_t>((qs * C::kQSlot) >> 4);
+      const uint64_t bk = dk0 + static_cast<uint64_t>((ks * C::kKVStage) >> 4);
 #pragma unroll
       for (int kk = 0; kk < D / 16; ++kk)
         mma_bf16_ss(d_s, aq + kmaj(kk), bk + kmaj(kk), kIdescS, kk > 0 ? 1u : 0u);
       mma_commit(&bar_s[t]);
     };
-    auto issue_pv = [&](int t, int vs, bool first) {
-      const uint32_t p_t = tmem + static_cast<uint32_t>(t) * BN;  // P_t over S_t
-      const uint32_t o_t = tmem + 2 * BN + static_cast<uint32_t>(t) * D;
+    auto issue_pv = [&](int vs, bool first) {
       // V tile [BN keys x D], D contiguous: MN-major B operand; LBO = distance
       // between the 64-wide column blocks of D; a k-step is 16 rows of 128 B
-      const uint64_t bv = dv0 + ((vs * C::kKVStage) >> 4);
+      const uint64_t bv = dv0 + static_cast<uint64_t>((vs * C::kKVStage) >> 4);
 #pragma unroll
       for (int kk = 0; kk < BN / 16; ++kk)
         mma_bf16_ts(o_t, p_t + kk * 8, bv + static_cast<uint64_t>((kk * 16 * 128) >> 4),
@@ -283,142 +324,301 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(
     auto wait_all = [&](uint64_t* bar, uint32_t parity) {
       return __all_sync(0xffffffffu, mbar_wait(bar, parity, &abort_flag));
     };
-
-    bool ok = wait_all(&bar_q, 0) && wait_all(&bar_kf[0], 0);
-    if (ok) {
-      tc_fence_after();
+    // release (commit) or give up (plain arrive) a slot of an empty barrier
+    auto release = [&](uint64_t* bar, bool used) {
       if (leader) {
-        issue_s(0, 0);
-        if (n_kv1 > 0) issue_s(1, 0);
-        mma_commit(&bar_ke[0]);
+        if (used)
+          mma_commit(bar);
+        else
+          mbar_arrive(bar);
       }
       __syncwarp();
-    }
-    for (int j = 0; ok && j < n_kv; ++j) {
-      const int vs = j % VS;
-      const int nx = j + 1;
-      const int ks = nx % KS;
-      ok = wait_all(&bar_vf[vs], (j / VS) & 1);
-      if (ok && nx < n_kv) ok = wait_all(&bar_kf[ks], (nx / KS) & 1);
-      for (int t = 0; ok && t < 2; ++t) {
-        const int n_t = t == 0 ? n_kv0 : n_kv1;
-        if (j >= n_t) continue;
-        ok = wait_all(&bar_p[t], j & 1);
+    };
+
+    int nu = 0, kb = 0;  // units and K/V tiles (of all units) consumed so far
+    int it = 0;          // (unit, K/V tile) steps of this query tile so far
+    bool ok = true;
+    for (int u = blockIdx.x; u < n_units && ok; u += gridDim.x, ++nu) {
+      const Unit w = decode_unit(u, n_ctiles, g, L, PM, CAUSAL, n_pairs, n_units);
+      const int n_kv = max(w.n0, w.n1);
+      const int n_me = t == 0 ? w.n0 : w.n1;
+      const int qs = nu % NQ;
+      if (n_me > 0) {
+        ok = wait_all(&bar_q[qs], (nu / NQ) & 1);
+        if (ok) ok = wait_all(&bar_kf[kb % KS], (kb / KS) & 1);
+        // S_t(0): with separate P the softmax must have read the previous S_t;
+        // with P inside S_t, the previous P_t.V was issued before (in order)
+        if (ok && kSepP && it > 0) ok = wait_all(&bar_sf[t], (it - 1) & 1);
         if (!ok) break;
         tc_fence_after();
-        if (leader) {
-          issue_pv(t, vs, j == 0);
-          if (nx < n_t) issue_s(t, ks);
-        }
+        if (leader) issue_s(qs, kb % KS);
         __syncwarp();
       }
-      if (!ok) break;
-      if (leader) {
-        mma_commit(&bar_ve[vs]);
-        if (nx < n_kv) mma_commit(&bar_ke[ks]);
+      // the query slot is free once this tile's last score product retires
+      if (n_me <= 1) release(&bar_qe[qs], n_me == 1);
+      for (int j = 0; ok && j < n_kv; ++j) {
+        const int kj = kb + j;  // ring index of K/V tile j
+        if (j >= n_me) {
+          // this query tile sees no keys from tile j on
+          release(&bar_ke[kj % KS], false);
+          release(&bar_ve[kj % VS], false);
+          continue;
+        }
+        const bool more = j + 1 < n_me;
+        if (kSepP) {
+          // K tile j: its score product was issued last step
+          release(&bar_ke[kj % KS], true);
+          if (more) {
+            // S_t(j+1) as soon as the softmax has read S_t(j)
+            ok = wait_all(&bar_kf[(kj + 1) % KS], ((kj + 1) / KS) & 1);
+            if (ok) ok = wait_all(&bar_sf[t], (it + j) & 1);
+            if (!ok) break;
+            tc_fence_after();
+            if (leader) issue_s(qs, (kj + 1) % KS);
+            __syncwarp();
+            if (j + 2 == n_me) release(&bar_qe[qs], true);
+          }
+          ok = wait_all(&bar_vf[kj % VS], (kj / VS) & 1);
+          if (ok) ok = wait_all(&bar_p[t], (it + j) & 1);
+          if (!ok) break;
+          tc_fence_after();
+          if (leader) issue_pv(kj % VS, j == 0);
+          __syncwarp();
+          release(&bar_ve[kj % VS], true);
+        } else {
+          // P_t(j) lives in S_t: P_t(j).V_j first, then S_t(j+1)
+          ok = wait_all(&bar_vf[kj % VS], (kj / VS) & 1);
+          if (ok) ok = wait_all(&bar_p[t], (it + j) & 1);
+          if (ok && more) ok = wait_all(&bar_kf[(kj + 1) % KS], ((kj + 1) / KS) & 1);
+          if (!ok) break;
+          tc_fence_after();
+          if (leader) {
+            issue_pv(kj % VS, j == 0);
+            if (more) issue_s(qs, (kj + 1) % KS);
+          }
+          __syncwarp();
+          if (more && j + 2 == n_me) release(&bar_qe[qs], true);
+          release(&bar_ke[kj % KS], true);
+          release(&bar_ve[kj % VS], true);
+        }
       }
-      __syncwarp();
+      if (!ok) break;
+      kb += n_kv;
+      it += n_me;
     }
     // every MMA must have retired before TMEM is released
     if (leader) {
-      mma_commit(&bar_fin);
-      mbar_drain(&bar_fin, 0);
+      mma_commit(&bar_fin[t]);
+      mbar_drain(&bar_fin[t], 0);
     }
     __syncwarp();
-  } else if (warp >= 4) {
+  }
+  } else {
+    setmaxnreg_inc<kRegsSoftmax>();
     // ------------------------------------------------------------ softmax
     const int t = (warp - 4) >> 2;  // query tile of this warpgroup
     const int wq = warp & 3;        // TMEM lane quadrant
     const int row = wq * 32 + lane;
-    const int pt = p0 + t * PM;
-    const int pos = pt + (row >> G_log2);
-    const int head = kvh * G + (row & (G - 1));
     const uint32_t lane_base = static_cast<uint32_t>(wq * 32) << 16;
     const uint32_t t_s = tmem + lane_base + static_cast<uint32_t>(t) * BN;
-    const uint32_t t_o = tmem + lane_base + 2 * BN + static_cast<uint32_t>(t) * D;
-    const int n_my = t == 0 ? n_kv0 : n_kv1;
-    // last key this row may see
-    const int last_key = CAUSAL ? min(L - 1, pos) : L - 1;
-    float m_run = -INFINITY;  // running max of scale*log2(e)*s, possibly stale by < 2^8
-    float l_run = 0.f;
+    const uint32_t t_o = tmem + lane_base + C::kColO + static_cast<uint32_t>(t) * D;
+    const uint32_t t_p = tmem + lane_base + C::kColP + static_cast<uint32_t>(t) * C::kStrideP;
+    const uint64_t c2 = f32x2(scale_log2, scale_log2);
+    int it = 0;     // (unit, K/V tile) steps of this query tile so far
+    int npass = 0;  // output staging passes of this query tile so far
+    int kturn = 0;  // exponential phases of both tiles in earlier units
     bool ok = true;
-    for (int j = 0; j < n_my; ++j) {
-      ok = __all_sync(0xffffffffu, mbar_wait(&bar_s[t], j & 1, &abort_flag));
-      if (!ok) break;
-      tc_fence_after();
-      const int key0 = j * BN;
-      const bool need_mask = (key0 + BN > L) || (CAUSAL && key0 + BN - 1 > pt);
-      const int nvis = last_key - key0;  // tile columns e <= nvis are visible
-      const float mx = need_mask ? tile_row_max<true>(t_s, nvis) : tile_row_max<false>(t_s, nvis);
-      const float m_new = fmaxf(m_run, mx * scale_log2);
-      if (__any_sync(0xffffffffu, m_new > m_run + kRescaleThreshold)) {
-        // the whole warp adopts its new maxima (tcgen05.ld/st are warp-wide)
-        const float alpha = m_run == -INFINITY ? 0.f : ex2_approx(m_run - m_new);
-        if (j > 0) {
-          // O_t holds keys < j*128 and no MMA writes it until P_t(j) is ready
-#pragma unroll
-          for (int c = 0; c < D / 32; ++c) {
-            uint32_t r[32];
-            tmem_ld32(t_o + c * 32, r);
-            tmem_ld_wait();
-#pragma unroll
-            for (int e = 0; e < 32; ++e) r[e] = __float_as_uint(__uint_as_float(r[e]) * alpha);
-            tmem_st32(t_o + c * 32, r);
-          }
-        }
-        l_run *= alpha;
-        m_run = m_new;
+    for (int u = blockIdx.x; u < n_units && ok; u += gridDim.x) {
+      const Unit w = decode_unit(u, n_ctiles, g, L, PM, CAUSAL, n_pairs, n_units);
+      const int n_my = t == 0 ? w.n0 : w.n1;
+      if (n_my == 0) {
+        kturn += w.n0 + w.n1;  // this tile sees no keys in this unit
+        continue;
       }
-      // P = 2^(s * scale * log2(e) - m_run) as bf16 pairs over S_t
-      l_run += need_mask ? tile_exp_to_p<true>(t_s, nvis, scale_log2, m_run)
-                         : tile_exp_to_p<false>(t_s, nvis, scale_log2, m_run);
-      tmem_st_wait();
-      tc_fence_before();
-      mbar_arrive(&bar_p[t]);
-    }
-    if (ok && n_my > 0)
-      ok = __all_sync(0xffffffffu, mbar_wait(&bar_o[t], (n_my - 1) & 1, &abort_flag));
-    if (ok && n_my > 0) {
-      tc_fence_after();
-      const bool store = pos < L;
-      const float inv_l = 1.f / l_run;
-      const size_t orow = (static_cast<size_t>(b) * L + pos) * h_q + head;
+      const int pt = w.p0 + t * PM;
+      const int pos = pt + (row >> G_log2);
+      const int head = w.kvh * G + (row & (G - 1));
+      const int last_key = CAUSAL ? min(L - 1, pos) : L - 1;  // last key this row may see
+      float m_run = -INFINITY;  // running max of scale*log2(e)*s, possibly stale by < 2^8
+      float l_run = 0.f;
+      for (int j = 0; j < n_my; ++j) {
+        ok = __all_sync(0xffffffffu, mbar_wait(&bar_s[t], (it + j) & 1, &abort_flag));
+        if (!ok) break;
+        tc_fence_after();
+        uint32_t r[BN];
 #pragma unroll
-      for (int c = 0; c < D / 32; ++c) {
-        uint32_t r[32];
-        tmem_ld32(t_o + c * 32, r);
+        for (int c = 0; c < BN / 32; ++c) tmem_ld32(t_s + c * 32, r + c * 32);
         tmem_ld_wait();
-        if (store) {
-          if (o_dtype == GQA_OUT_F32) {
-            float4* dst = reinterpret_cast<float4*>(static_cast<float*>(o) + orow * D + c * 32);
+        if (kSepP) {
+          // S_t may be overwritten by the next score product from here on
+          tc_fence_before();
+          mbar_arrive(&bar_sf[t]);
+        }
+        const int key0 = j * BN;
+        const bool need_mask = (key0 + BN > L) || (CAUSAL && key0 + BN - 1 > pt);
+        if (need_mask) {
+          const int nvis = last_key - key0;  // tile columns e <= nvis are visible
 #pragma unroll
-            for (int e = 0; e < 8; ++e)
-              dst[e] = make_float4(__uint_as_float(r[4 * e]) * inv_l,
-                                   __uint_as_float(r[4 * e + 1]) * inv_l,
-                                   __uint_as_float(r[4 * e + 2]) * inv_l,
-                                   __uint_as_float(r[4 * e + 3]) * inv_l);
-          } else {
-            uint4* dst =
-                reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(o) + orow * D + c * 32);
+          for (int e = 0; e < BN; ++e)
+            if (e > nvis) r[e] = 0xff800000u;  // -inf
+        }
+        // row max (three-input max, four independent chains)
+        float mx4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll
-            for (int e = 0; e < 4; ++e) {
-              uint32_t wv[4];
+        for (int e = 0; e < BN / 2; ++e)
+          mx4[e & 3] = max3f(mx4[e & 3], __uint_as_float(r[2 * e]), __uint_as_float(r[2 * e + 1]));
+        const float mx = max3f(mx4[0], mx4[1], fmaxf(mx4[2], mx4[3]));
+        const float m_new = fmaxf(m_run, mx * scale_log2);
+        const bool rescale = __any_sync(0xffffffffu, m_new > m_run + kRescaleThreshold);
+        float alpha = 1.f;
+        if (rescale) {
+          // the whole warp adopts its new maxima (tcgen05.ld/st are warp-wide)
+          alpha = m_run == -INFINITY ? 0.f : ex2_approx(m_run - m_new);
+          l_run *= alpha;
+          m_run = m_new;
+        }
+        if (j > 0) {
+          // P_t(j-1).V_{j-1} has retired: O_t holds keys < j*128 and, with
+          // separate P, the P_t columns are free again
+          ok = __all_sync(0xffffffffu, mbar_wait(&bar_o[t], (it + j - 1) & 1, &abort_flag));
+          if (!ok) break;
+          tc_fence_after();
+          if (rescale) {
+            // rare (lazy rescale); small chunks keep the score registers live
+#pragma unroll 1
+            for (int c = 0; c < D / 8; ++c) {
+              uint32_t ov[8];
+              tmem_ld8(t_o + c * 8, ov);
+              tmem_ld_wait();
 #pragma unroll
-              for (int q = 0; q < 4; ++q) {
-                const float lo = __uint_as_float(r[8 * e + 2 * q]) * inv_l;
-                const float hi = __uint_as_float(r[8 * e + 2 * q + 1]) * inv_l;
-                __nv_bfloat162 v2 = __floats2bfloat162_rn(lo, hi);
-                wv[q] = *reinterpret_cast<uint32_t*>(&v2);
-              }
-              dst[e] = make_uint4(wv[0], wv[1], wv[2], wv[3]);
+              for (int e = 0; e < 8; ++e)
+                ov[e] = __float_as_uint(__uint_as_float(ov[e]) * alpha);
+              tmem_st8(t_o + c * 8, ov);
             }
           }
         }
+        // The two softmax warps that share an SM sub-partition (warp 4+q of
+        // tile 0, warp 8+q of tile 1) take turns on the exponential unit, in
+        // the order (step j, tile 0), (step j, tile 1), (step j+1, tile 0)...:
+        // one warp's exponentials overlap the other's loads, max and waits
+        // instead of both halving each other's throughput. Phase k waits for
+        // phase k-1 (of either warp; phase k+1 cannot have started).
+        const int kt = kturn + min(j, w.n0) + min(j, w.n1) + (t == 1 && j < w.n0 ? 1 : 0);
+        if (kt > 0) {
+          ok = mbar_wait(&bar_turn[wq], (kt - 1) & 1, &abort_flag);
+          ok = __all_sync(0xffffffffu, ok);
+          if (!ok) break;
+        }
+        // P = 2^(s * scale * log2(e) - m_run) as bf16 pairs, 64 keys at a time;
+        // scale-and-shift and the running sum use packed two-lane fp32 ops
+        const uint64_t nm2 = f32x2(-m_run, -m_run);
+        uint64_t sum2[2] = {0ull, 0ull};
+#pragma unroll
+        for (int hh = 0; hh < 2; ++hh) {
+          uint32_t pw[32];
+#pragma unroll
+          for (int e = 0; e < 32; ++e) {
+            const int c = hh * 64 + 2 * e;
+            float xa, xb;
+            split_f32x2(ffma_x2(u32x2(r[c], r[c + 1]), c2, nm2), xa, xb);
+            const float pa = ex2_approx(xa);
+            const float pb = ex2_approx(xb);
+            sum2[e & 1] = fadd_x2(sum2[e & 1], f32x2(pa, pb));
+            pw[e] = pack_bf16x2(pa, pb);
+          }
+          tmem_st32(t_p + hh * 32, pw);  // P columns [32hh, 32hh+32) = keys [64hh, 64hh+64)
+        }
+        mbar_arrive(&bar_turn[wq]);  // this warp's exponential phase is over
+        tmem_st_wait();
+        tc_fence_before();
+        mbar_arrive(&bar_p[t]);
+        float a0, a1, b0, b1;
+        split_f32x2(sum2[0], a0, a1);
+        split_f32x2(sum2[1], b0, b1);
+        l_run += (a0 + a1) + (b0 + b1);
       }
+      if (!ok) break;
+      // epilogue: O_t is final once the last P_t.V retires
+      ok = __all_sync(0xffffffffu, mbar_wait(&bar_o[t], (it + n_my - 1) & 1, &abort_flag));
+      if (!ok) break;
+      tc_fence_after();
+      it += n_my;
+      kturn += w.n0 + w.n1;
+      const float inv_l = 1.f / l_run;
+      // O_t / l: staged in shared memory (128-byte swizzle, so the row-per-
+      // thread writes spread over all banks) and stored by TMA in 128-byte
+      // column chunks; rows past L are dropped by the store itself
+      const bool f32 = o_dtype == GQA_OUT_F32;
+      const int n_chunks = f32 ? D / 32 : D / 64;
+      const bool wg_leader = threadIdx.x == 128 + 128 * t;
+      uint8_t* stage = smem + C::kOffStage + t * C::kStageBytes;
+      const uint32_t sw = static_cast<uint32_t>(row & 7);
+      // staging hand-off through mbarriers (bounded waits): bar_stf[t] phase
+      // k = the stage is free again after pass k, bar_stw[t] phase k = every
+      // thread has written its rows for pass k
+      for (int c0 = 0; c0 < n_chunks && ok; c0 += C::kStageChunks, ++npass) {
+        if (npass > 0) {
+          if (wg_leader) {
+            bulk_wait_read_all();  // the previous pass's stores have read the stage
+            mbar_arrive(&bar_stf[t]);
+          }
+          ok = mbar_wait(&bar_stf[t], (npass - 1) & 1, &abort_flag);
+          if (!ok) break;
+        }
+#pragma unroll
+        for (int cc = 0; cc < C::kStageChunks; ++cc) {
+          const int chunk = c0 + cc;
+          if (chunk >= n_chunks) break;
+          uint8_t* dst = stage + cc * C::kChunkBytes + row * 128;
+          if (f32) {
+            uint32_t rr[32];
+            tmem_ld32(t_o + chunk * 32, rr);
+            tmem_ld_wait();
+#pragma unroll
+            for (int u4 = 0; u4 < 8; ++u4)
+              *reinterpret_cast<float4*>(dst + ((u4 ^ sw) << 4)) =
+                  make_float4(__uint_as_float(rr[4 * u4]) * inv_l,
+                              __uint_as_float(rr[4 * u4 + 1]) * inv_l,
+                              __uint_as_float(rr[4 * u4 + 2]) * inv_l,
+                              __uint_as_float(rr[4 * u4 + 3]) * inv_l);
+          } else {
+#pragma unroll
+            for (int hh = 0; hh < 2; ++hh) {
+              uint32_t rr[32];
+              tmem_ld32(t_o + chunk * 64 + hh * 32, rr);
+              tmem_ld_wait();
+#pragma unroll
+              for (int u4 = 0; u4 < 4; ++u4) {
+                uint32_t wv[4];
+#pragma unroll
+                for (int q2 = 0; q2 < 4; ++q2)
+                  wv[q2] = pack_bf16x2(__uint_as_float(rr[8 * u4 + 2 * q2]) * inv_l,
+                                       __uint_as_float(rr[8 * u4 + 2 * q2 + 1]) * inv_l);
+                *reinterpret_cast<uint4*>(dst + (((hh * 4 + u4) ^ sw) << 4)) =
+                    make_uint4(wv[0], wv[1], wv[2], wv[3]);
+              }
+            }
+          }
+        }
+        fence_proxy_async_smem();  // the generic-proxy writes become visible to TMA
+        mbar_arrive(&bar_stw[t]);
+        if (wg_leader) {
+          ok = mbar_wait(&bar_stw[t], npass & 1, &abort_flag);
+          if (ok) {
+            for (int cc = 0; cc < C::kStageChunks && c0 + cc < n_chunks; ++cc)
+              tma_store_4d(&tm_o, stage + cc * C::kChunkBytes, (c0 + cc) * (f32 ? 32 : 64),
+                           w.kvh * G, pt, w.b);
+            bulk_commit_group();
+          }
+        }
+      }
+      if (!ok) break;
+      const bool store = pos < L;
       if (lse != nullptr && store)
-        lse[(static_cast<size_t>(b) * h_q + head) * L + pos] =
+        lse[(static_cast<size_t>(w.b) * h_q + head) * L + pos] =
             (m_run + __log2f(l_run)) * 0.69314718055994531f;
     }
+    if (threadIdx.x == 128 + 128 * t) bulk_wait_all();  // output stores complete
   }
 
   tc_fence_before();
@@ -431,22 +631,43 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(
   if (threadIdx.x == 0 && abort_flag) record_status(status, GQA_ERR_TIMEOUT);
 }
 
+namespace {
+
+int sm_count() {
+  static int n = 0;  // one device per process in practice; re-queried if unset
+  if (n == 0) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n < 1)
+      n = 148;
+  }
+  return n;
+}
+
+}  // namespace
+
 template <int D, bool CAUSAL>
 static cudaError_t launch_prefill_t(const PrefillArgs& a, cudaStream_t s) {
   constexpr uint32_t kSmem = PrefillCfg<D>::kSmem;
   static bool attr_set = false;
   if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(prefill_kernel<D, CAUSAL>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
+    // the register hand-over inside the kernel assumes the launch pool
+    cudaFuncAttributes fa{};
+    cudaError_t e = cudaFuncGetAttributes(&fa, prefill_kernel<D, CAUSAL>);
+    if (e != cudaSuccess) return e;
+    if (fa.numRegs != kRegsLaunch) return cudaErrorInvalidKernelImage;
+    e = cudaFuncSetAttribute(prefill_kernel<D, CAUSAL>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
     if (e != cudaSuccess) return e;
     attr_set = true;
   }
   const int PM = BM / a.G;
   const int n_ctiles = (a.L + 2 * PM - 1) / (2 * PM);
-  dim3 grid(n_ctiles, a.g, a.B);
+  const long long n_units = static_cast<long long>(n_ctiles) * a.g * a.B;
+  const int grid = static_cast<int>(n_units < sm_count() ? n_units : sm_count());
   prefill_kernel<D, CAUSAL><<<grid, kThreads, kSmem, s>>>(
-      a.tm_q, a.tm_k, a.tm_v, a.o, a.o_dtype, a.lse, a.L, a.h_q, a.G, a.G_log2, a.scale_log2,
-      n_ctiles, a.status);
+      a.tm_q, a.tm_k, a.tm_v, a.tm_o, a.o_dtype, a.lse, a.B, a.L, a.h_q, a.g, a.G, a.G_log2,
+      a.scale_log2, n_ctiles, static_cast<int>(n_units), a.status);
   return cudaGetLastError();
 }
 
