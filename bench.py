@@ -270,7 +270,8 @@ def native_arm(args):
     ws = torch.empty(gqa.gqa_decode_workspace_bytes(B, h_q, g, d, S_max), dtype=torch.uint8,
                      device=dev)
     status = torch.zeros(1, dtype=torch.int32, device=dev)
-    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    from grouped_query_attention_10_b300.run_workload import make_l2_flush
+    flush = make_l2_flush(dev)
     stream = torch.cuda.current_stream(dev)
 
     flops_prefill = accounting.prefill_flops(B, L, h_q, d, w.causal)
@@ -291,7 +292,7 @@ def native_arm(args):
                            status=status, stream=stream)
 
     for _ in range(max(args.warmup, 3)):
-        flush.zero_()
+        flush()
         step()
     torch.cuda.synchronize()
 
@@ -300,7 +301,7 @@ def native_arm(args):
     torch.cuda.synchronize()
     with ClockSampler(local) as clk:
         for i in range(args.steps):
-            flush.zero_()  # L2 flush between timed steps, outside the timed interval
+            flush()  # L2 flush between timed steps, outside the timed interval
             e0, ep0, ep1, e1 = evs[i]
             e0.record(stream)
             step(ep0, ep1)
@@ -373,7 +374,7 @@ def native_arm(args):
         "config": {"workload": "gqa_step_noncausal_b32_l1024_hq8_g4_d64",
                    "B": B, "L": L, "h_q": h_q, "g": g, "d": d, "causal": False,
                    "step": "append prompt K/V, prefill, append 1 token, decode 1 token",
-                   "l2": "flushed between timed steps (256 MiB write)",
+                   "l2": "flushed between timed steps (256 MiB write, then 256 MiB read)",
                    "parallelism": f"replicas x{world}"},
         "roofline": roofline,
         "e2e": e2e,
@@ -401,7 +402,7 @@ def _time_calls(fn, n, stream, flush=None):
            for _ in range(n)]
     for a, b in evs:
         if flush is not None:
-            flush.zero_()
+            flush()
         a.record(stream)
         fn()
         b.record(stream)
@@ -437,7 +438,8 @@ def extra_measurements(dev, stream, peaks, peak_src):
         o = torch.empty((w.B, w.h_q, w.d), dtype=torch.float32, device=dev)
         ws = torch.empty(gqa.gqa_decode_workspace_bytes(w.B, w.h_q, w.g, w.d, w.S_max),
                          dtype=torch.uint8, device=dev)
-        flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+        from grouped_query_attention_10_b300.run_workload import make_l2_flush
+        flush = make_l2_flush(dev)
         fn = lambda: gqa.gqa_decode_fwd(q, kc, vc, lens, scale=w.scale, out=o, workspace=ws,
                                         stream=stream)
         _time_calls(fn, 3, stream, flush)

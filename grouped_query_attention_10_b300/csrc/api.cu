@@ -73,26 +73,28 @@ constexpr long long kMaxElems = 1LL << 40;
 
 struct DecodeLayout {
   int split_len, n_split;
-  size_t part_o_bytes, part_lse_off, total;
+  size_t part_o_bytes, part_lse_off, counter_off, total;
 };
 
 DecodeLayout decode_layout(int B, int h_q, int g, int d, int S_max) {
   DecodeLayout l{};
-  l.split_len = gqa::decode_split_len(B, g, S_max);
+  l.split_len = gqa::decode_split_len(B, h_q, g, S_max);
   l.n_split = (S_max + l.split_len - 1) / l.split_len;
-  const size_t rows = static_cast<size_t>(B) * h_q * l.n_split;
+  const size_t rows = static_cast<size_t>(B) * h_q * l.n_split * gqa::kDecodeSlices;
   l.part_o_bytes = rows * d * sizeof(float);
   l.part_lse_off = (l.part_o_bytes + 255) & ~static_cast<size_t>(255);
-  l.total = l.part_lse_off + rows * sizeof(float);
+  l.counter_off = (l.part_lse_off + rows * sizeof(float) + 255) & ~static_cast<size_t>(255);
+  l.total = l.counter_off + 16;
   return l;
 }
 
 bool decode_shape_ok(int B, int h_q, int g, int d, int S_max) {
   if (B < 1 || B > 65535 || S_max < 1 || !heads_ok(h_q, g, d)) return false;
   const long long G = h_q / g;
-  if (static_cast<long long>(g) * ((G + 31) / 32) > 65535) return false;
   if (static_cast<long long>(B) * g * S_max * d >= kMaxElems) return false;
-  if (static_cast<long long>(B) * g >= (1LL << 31)) return false;
+  // work items (64-token stages at the finest split) index an int
+  if (static_cast<long long>(B) * g * ((G + 31) / 32) * (S_max / 64 + 1) >= (1LL << 31))
+    return false;
   return true;
 }
 
@@ -222,6 +224,7 @@ int gqa_decode_fwd(const void* q, const void* k_cache, const void* v_cache,
   a.lse = lse;
   a.part_o = static_cast<float*>(workspace);
   a.part_lse = reinterpret_cast<float*>(static_cast<char*>(workspace) + lay.part_lse_off);
+  a.item_counter = reinterpret_cast<int*>(static_cast<char*>(workspace) + lay.counter_off);
   a.B = B;
   a.h_q = h_q;
   a.g = g;

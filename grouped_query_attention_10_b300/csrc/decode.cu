@@ -5,13 +5,16 @@
 // K/V row. Design (split-KV, the split attention forward sketched in the
 // "Qwen, DeepSeek and LLaMA3 attention survey" (jsqmd.com), chapter 5):
 //
-//  * pass 1 (decode_split_kernel): one CTA per (split, kv head, sequence).
-//    It streams its split of the K and V rows through a TMA-fed shared-memory
-//    ring (128-byte swizzle, so ldmatrix reads are bank-conflict free) and
-//    serves ALL G = h_q/g query heads of the group from the same bytes: the G
-//    query rows are stacked as the M side of m16n8k16 tensor-core MMAs. Each
-//    K/V byte is read from HBM once per K/V head, never once per query head.
-//    The CTA writes its normalised partial output and its log2 sum-exp.
+//  * pass 1 (decode_split_kernel): the work items are (split, slice of the
+//    group's query heads, K/V head, sequence); persistent CTAs (two per SM)
+//    walk them. A producer warp streams each item's K and V rows through a
+//    TMA-fed shared-memory ring (128-byte swizzle, so ldmatrix reads are
+//    bank-conflict free); the ring carries on from one item to the next.
+//    Four consumer warps serve ALL query heads of the group from the same
+//    bytes: the heads are stacked as the M side of m16n8k16 tensor-core
+//    MMAs, so each K/V byte is read from HBM once per K/V head, never once
+//    per query head. Every item ends with its normalised partial output and
+//    its log2 sum-exp.
 //  * pass 2 (decode_combine_kernel): log-sum-exp combine of the partials.
 #include <cuda_bf16.h>
 
@@ -23,8 +26,20 @@ namespace gqa {
 
 namespace {
 
-constexpr int kStages = 2;     // ring depth (stages of kDecodeStage tokens)
-constexpr int kThreads = 128;  // 4 warps
+constexpr int kConsumers = 4;                    // consumer warps
+constexpr int kThreads = 32 * (kConsumers + 1);  // + one producer warp
+constexpr int kCtasPerSm = 2;
+constexpr float kRescaleThreshold = 8.0f;  // log2 units
+
+template <int D>
+struct DecCfg {
+  static constexpr int kStages = D == 128 ? 3 : 6;         // ring depth (96 KB)
+  static constexpr int kCB = D / 64;                        // 64-wide column blocks
+  static constexpr int kBoxBytes = kDecodeStage * 128;      // 64 rows x 128 B
+  static constexpr int kStageBytes = 2 * kCB * kBoxBytes;   // K + V
+  static constexpr int kRing = kStages * kStageBytes;
+  static constexpr int kSmem = kRing + 1024;                // + alignment slack
+};
 
 __device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2,
                                         uint32_t& r3) {
@@ -55,202 +70,291 @@ __device__ __forceinline__ uint32_t sw128(int row, int chunk) {
   return static_cast<uint32_t>(row * 128 + ((chunk ^ (row & 7)) << 4));
 }
 
+// One decoded work item.
+struct Item {
+  int b, kvh, hs, split;
+  int s0, s1, n_st;  // token range [s0, s1) and its 64-token stages (0: nothing to do)
+};
+
+// Items are numbered split-major (every segment's first split, then every
+// segment's second split, ...): items are fetched in that order, so the
+// partial and empty splits at the end of short sequences come last and fill
+// the tail of the pass.
+__device__ __forceinline__ Item decode_item(int u, const int32_t* seq_lens, int g, int n_hslice,
+                                            int S_max, int split_len, int n_segs) {
+  Item it;
+  it.split = u / n_segs;
+  const int seg = u % n_segs;
+  it.hs = seg % n_hslice;
+  const int pair = seg / n_hslice;
+  it.kvh = pair % g;
+  it.b = pair / g;
+  int len = seq_lens[it.b];
+  len = len < 0 ? 0 : (len > S_max ? S_max : len);
+  it.s0 = it.split * split_len;
+  it.s1 = min(len, it.s0 + split_len);
+  it.n_st = it.s0 < len ? (it.s1 - it.s0 + kDecodeStage - 1) / kDecodeStage : 0;
+  return it;
+}
+
 }  // namespace
 
 // D: head dim (64 or 128). MT: m16 tiles of stacked query rows (G <= 16*MT).
 template <int D, int MT>
-__global__ void __launch_bounds__(kThreads) decode_split_kernel(
+__global__ void __launch_bounds__(kThreads, kCtasPerSm) decode_split_kernel(
     const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
     const __nv_bfloat16* __restrict__ q, const int32_t* __restrict__ seq_lens,
     float* __restrict__ part_o, float* __restrict__ part_lse, int h_q, int g, int G,
-    int n_hslice, int S_max, int split_len, int n_split, float scale_log2, int32_t* status) {
-  constexpr int kBoxBytes = kDecodeStage * 128;       // 64 rows x 128 B
-  constexpr int kCB = D / 64;                         // 64-wide column blocks
-  constexpr int kStageBytes = 2 * kCB * kBoxBytes;    // K + V
-  constexpr int kNSlices = 4 / MT;                    // warps sharing one m-tile
+    int n_hslice, int S_max, int split_len, int n_split, int n_items, float scale_log2,
+    int* __restrict__ item_counter, int32_t* status) {
+  using C = DecCfg<D>;
+  constexpr int kStages = C::kStages;
+  constexpr int kCB = C::kCB;
+  constexpr int kNSlices = kConsumers / MT;                // warps sharing one m-tile
   constexpr int kSubPerWarp = (kDecodeStage / 16) / kNSlices;
 
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
   __shared__ __align__(8) uint64_t full_bar[kStages];
+  __shared__ __align__(8) uint64_t empty_bar[kStages];   // one arrival per consumer warp
+  __shared__ int4 tag[kStages];              // item, stage, stages of the item (item < 0: end)
   __shared__ int abort_flag;
 
-  const int split = blockIdx.x;
-  const int kvh = blockIdx.y / n_hslice;
-  const int hs = blockIdx.y % n_hslice;  // 32-row slice of the group (G > 32 only)
-  const int b = blockIdx.z;
   const int tid = threadIdx.x;
   const int warp = tid >> 5;
   const int lane = tid & 31;
 
-  int len = seq_lens[b];
-  if (len < 0 || len > S_max) {
-    if (tid == 0 && split == 0 && kvh == 0) record_status(status, GQA_ERR_BAD_LENGTH);
-    len = len < 0 ? 0 : S_max;
-  }
-  const int s0 = split * split_len;
-  if (s0 >= len) return;  // the combine pass ignores splits past the length
-  const int s1 = min(len, s0 + split_len);
-  const int n_st = (s1 - s0 + kDecodeStage - 1) / kDecodeStage;
-  const int zrow = b * g + kvh;
-
   if (tid == 0) {
     abort_flag = 0;
-    for (int i = 0; i < kStages; ++i) mbar_init(&full_bar[i], 1);
+    for (int i = 0; i < kStages; ++i) {
+      mbar_init(&full_bar[i], 1);
+      mbar_init(&empty_bar[i], kConsumers);
+    }
     fence_mbar_init();
   }
   __syncthreads();
 
-  auto issue_stage = [&](int st) {
-    const int slot = st % kStages;
-    uint8_t* base = smem + slot * kStageBytes;
-    const int y = s0 + st * kDecodeStage;
-    mbar_arrive_expect_tx(&full_bar[slot], kStageBytes);
+  if (warp == kConsumers) {
+    // ---------------------------------------------------------------- producer
+    if (lane == 0) {
+      prefetch_tmap(&tm_k);
+      prefetch_tmap(&tm_v);
+      const int n_segs = n_items / n_split;
+      int sc = 0;  // stages issued so far
+      bool ok = true;
+      // items are fetched from a counter the host zeroes before the launch,
+      // so CTAs that drew short items simply fetch more
+      for (int u = atomicAdd(item_counter, 1); u < n_items && ok;
+           u = atomicAdd(item_counter, 1)) {
+        const Item it = decode_item(u, seq_lens, g, n_hslice, S_max, split_len, n_segs);
+        const int zrow = it.b * g + it.kvh;
+        for (int st = 0; st < it.n_st; ++st, ++sc) {
+          const int slot = sc % kStages;
+          if (sc >= kStages) ok = mbar_wait(&empty_bar[slot], ((sc / kStages) - 1) & 1, &abort_flag);
+          if (!ok) break;
+          tag[slot] = make_int4(u, st, it.n_st, 0);
+          uint8_t* base = smem + slot * C::kStageBytes;
+          const int y = it.s0 + st * kDecodeStage;
+          mbar_arrive_expect_tx(&full_bar[slot], C::kStageBytes);
 #pragma unroll
-    for (int cb = 0; cb < kCB; ++cb) {
-      tma_load_3d(base + cb * kBoxBytes, &tm_k, &full_bar[slot], cb * 64, y, zrow);
-      tma_load_3d(base + (kCB + cb) * kBoxBytes, &tm_v, &full_bar[slot], cb * 64, y, zrow);
-    }
-  };
-  if (tid == 0) {
-    prefetch_tmap(&tm_k);
-    prefetch_tmap(&tm_v);
-    for (int st = 0; st < kStages && st < n_st; ++st) issue_stage(st);
-  }
-
-  // ---- this warp's stacked query rows as m16n8k16 A fragments
-  const int mt = warp % MT;
-  const int slice = warp / MT;
-  const int gr = lane >> 2;  // fragment row group
-  const int tq = lane & 3;   // fragment column pair
-  const int row0 = mt * 16 + gr;
-  const int row1 = row0 + 8;
-  const size_t head0 = static_cast<size_t>(b) * h_q + static_cast<size_t>(kvh) * G + hs * 32;
-  const int Gs = min(G - hs * 32, 16 * MT);  // stacked rows served by this CTA
-  const __nv_bfloat16* qg = q + head0 * D;
-  uint32_t qa[D / 16][4];
-#pragma unroll
-  for (int kk = 0; kk < D / 16; ++kk) {
-    const int c = kk * 16 + tq * 2;
-    qa[kk][0] = row0 < Gs ? *reinterpret_cast<const uint32_t*>(qg + row0 * D + c) : 0u;
-    qa[kk][1] = row1 < Gs ? *reinterpret_cast<const uint32_t*>(qg + row1 * D + c) : 0u;
-    qa[kk][2] = row0 < Gs ? *reinterpret_cast<const uint32_t*>(qg + row0 * D + c + 8) : 0u;
-    qa[kk][3] = row1 < Gs ? *reinterpret_cast<const uint32_t*>(qg + row1 * D + c + 8) : 0u;
-  }
-
-  float o_acc[D / 8][4];
-#pragma unroll
-  for (int i = 0; i < D / 8; ++i) o_acc[i][0] = o_acc[i][1] = o_acc[i][2] = o_acc[i][3] = 0.f;
-  float m_r[2] = {-INFINITY, -INFINITY};
-  float l_r[2] = {0.f, 0.f};
-
-  const uint32_t smem_base = smem_u32(smem);
-  bool ok = true;
-  for (int st = 0; st < n_st && ok; ++st) {
-    const int slot = st % kStages;
-    // every thread waits; the vote keeps `ok` uniform across the CTA so the
-    // barriers below are never reached by only part of it
-    ok = __syncthreads_and(mbar_wait(&full_bar[slot], (st / kStages) & 1, &abort_flag) ? 1 : 0);
-    const int tok0 = s0 + st * kDecodeStage;
-    const int valid = s1 - tok0;  // rows of this stage that are real
-    const uint32_t kbase = smem_base + slot * kStageBytes;
-    const uint32_t vbase = kbase + kCB * kBoxBytes;
-    if (ok && valid < kDecodeStage) {
-      // rows past the sequence may hold anything (even NaN); 0 * NaN would
-      // poison P.V, so zero those V rows before any warp reads them
-      uint8_t* vrows = smem + slot * kStageBytes + kCB * kBoxBytes;
-      for (int i = tid; i < (kDecodeStage - valid) * kCB * 8; i += kThreads) {
-        const int r = valid + i / (kCB * 8);
-        const int cb = (i / 8) % kCB;
-        const int ch = i % 8;
-        *reinterpret_cast<uint4*>(vrows + cb * kBoxBytes + r * 128 + ch * 16) =
-            make_uint4(0u, 0u, 0u, 0u);
+          for (int cb = 0; cb < kCB; ++cb) {
+            tma_load_3d(base + cb * C::kBoxBytes, &tm_k, &full_bar[slot], cb * 64, y, zrow);
+            tma_load_3d(base + (kCB + cb) * C::kBoxBytes, &tm_v, &full_bar[slot], cb * 64, y,
+                        zrow);
+          }
+        }
       }
-      __syncthreads();
+      if (ok) {
+        // end marker: a slot with no data and a negative item
+        const int slot = sc % kStages;
+        if (sc >= kStages) ok = mbar_wait(&empty_bar[slot], ((sc / kStages) - 1) & 1, &abort_flag);
+        if (ok) {
+          tag[slot] = make_int4(-1, 0, 0, 0);
+          mbar_arrive(&full_bar[slot]);
+        }
+      }
+      if (!ok) {
+        // every issued copy must land before the CTA may exit
+        for (int s = 0; s < kStages && s < sc; ++s) {
+          const int last = s + ((sc - 1 - s) / kStages) * kStages;
+          mbar_drain(&full_bar[s], (last / kStages) & 1);
+        }
+      }
     }
-    if (ok) {
+  } else {
+    // ---------------------------------------------------------------- consumers
+    const int mt = warp % MT;
+    const int slice = warp / MT;
+    const int gr = lane >> 2;  // fragment row group
+    const int tq = lane & 3;   // fragment column pair
+    const int row0 = mt * 16 + gr;
+    const int row1 = row0 + 8;
+    const uint32_t smem_base = smem_u32(smem);
+    const int n_segs = n_items / n_split;
+    int sc = 0;  // stages consumed so far
+    bool ok = true;
+    Item it{};
+    size_t head0 = 0;
+    int Gs = 0;
+    uint32_t qa[D / 16][4];
+    float o_acc[D / 8][4];
+    float m_r[2] = {-INFINITY, -INFINITY};  // running max (log2 units), stale by < 2^8
+    float l_r[2] = {0.f, 0.f};
+    while (ok) {
+      const int slot = sc % kStages;
+      ok = __all_sync(0xffffffffu, mbar_wait(&full_bar[slot], (sc / kStages) & 1, &abort_flag));
+      if (!ok) break;
+      const int4 tg = tag[slot];
+      if (tg.x < 0) break;  // no more items
+      const int st = tg.y;
+      if (st == 0) {
+        // a new item: its query rows and fresh accumulators
+        it = decode_item(tg.x, seq_lens, g, n_hslice, S_max, split_len, n_segs);
+        head0 = static_cast<size_t>(it.b) * h_q + static_cast<size_t>(it.kvh) * G + it.hs * 32;
+        Gs = min(G - it.hs * 32, 16 * MT);  // stacked rows served by this item
+        const __nv_bfloat16* qg = q + head0 * D;
 #pragma unroll
-      for (int sbi = 0; sbi < kSubPerWarp; ++sbi) {
-        const int r0 = (slice + sbi * kNSlices) * 16;  // first row of this 16-token block
-        float s[2][4];
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const int c = kk * 16 + tq * 2;
+          qa[kk][0] = row0 < Gs ? *reinterpret_cast<const uint32_t*>(qg + row0 * D + c) : 0u;
+          qa[kk][1] = row1 < Gs ? *reinterpret_cast<const uint32_t*>(qg + row1 * D + c) : 0u;
+          qa[kk][2] = row0 < Gs ? *reinterpret_cast<const uint32_t*>(qg + row0 * D + c + 8) : 0u;
+          qa[kk][3] = row1 < Gs ? *reinterpret_cast<const uint32_t*>(qg + row1 * D + c + 8) : 0u;
+        }
 #pragma unroll
-        for (int j = 0; j < 2; ++j) s[j][0] = s[j][1] = s[j][2] = s[j][3] = 0.f;
+        for (int i = 0; i < D / 8; ++i) o_acc[i][0] = o_acc[i][1] = o_acc[i][2] = o_acc[i][3] = 0.f;
+        m_r[0] = m_r[1] = -INFINITY;
+        l_r[0] = l_r[1] = 0.f;
+      }
+      const int tok0 = it.s0 + st * kDecodeStage;
+      const int valid = it.s1 - tok0;  // rows of this stage that are real
+      const uint32_t kbase = smem_base + slot * C::kStageBytes;
+      const uint32_t vbase = kbase + kCB * C::kBoxBytes;
+      // This warp's 16-token blocks of the stage are processed together (their
+      // score products form independent MMA chains), with one max / sum
+      // reduction and one rescale decision for all of them.
+      int r0[kSubPerWarp];
+      bool act[kSubPerWarp];
+#pragma unroll
+      for (int sb = 0; sb < kSubPerWarp; ++sb) {
+        r0[sb] = (slice + sb * kNSlices) * 16;  // first row of the 16-token block
+        act[sb] = r0[sb] < valid;               // any real token in it
+        if (act[sb] && r0[sb] + 16 > valid) {
+          // rows past the sequence may hold anything (even NaN) and 0 * NaN
+          // would poison P.V: zero this block's V rows past the end. Only the
+          // warps that read these rows write them, and all write zeros.
+          uint8_t* vrows = smem + slot * C::kStageBytes + kCB * C::kBoxBytes;
+          for (int i = lane; i < 16 * kCB * 8; i += 32) {
+            const int r = r0[sb] + i / (kCB * 8);
+            const int cb = (i / 8) % kCB;
+            const int ch = i % 8;
+            if (r >= valid)
+              *reinterpret_cast<uint4*>(vrows + cb * C::kBoxBytes + r * 128 + ch * 16) =
+                  make_uint4(0u, 0u, 0u, 0u);
+          }
+          __syncwarp();
+        }
+      }
+      if (act[0]) {
+        float s[kSubPerWarp][2][4];
+#pragma unroll
+        for (int sb = 0; sb < kSubPerWarp; ++sb)
+#pragma unroll
+          for (int j = 0; j < 2; ++j) s[sb][j][0] = s[sb][j][1] = s[sb][j][2] = s[sb][j][3] = 0.f;
         // S = Q K^T over d
         {
           const int mi = lane >> 3;
           const int ri = lane & 7;
-          const int tok = r0 + (mi >> 1) * 8 + ri;
 #pragma unroll
           for (int kk = 0; kk < D / 16; ++kk) {
             const int chunk = (kk * 2 + (mi & 1)) & 7;
-            const uint32_t addr = kbase + (kk >> 2) * kBoxBytes + sw128(tok, chunk);
-            uint32_t b0, b1, b2, b3;
-            ldsm_x4(addr, b0, b1, b2, b3);
-            mma16816(s[0], qa[kk], b0, b1);
-            mma16816(s[1], qa[kk], b2, b3);
+#pragma unroll
+            for (int sb = 0; sb < kSubPerWarp; ++sb) {
+              if (!act[sb]) continue;
+              const int tok = r0[sb] + (mi >> 1) * 8 + ri;
+              const uint32_t addr = kbase + (kk >> 2) * C::kBoxBytes + sw128(tok, chunk);
+              uint32_t b0, b1, b2, b3;
+              ldsm_x4(addr, b0, b1, b2, b3);
+              mma16816(s[sb][0], qa[kk], b0, b1);
+              mma16816(s[sb][1], qa[kk], b2, b3);
+            }
           }
         }
         // mask, scale to log2 units, online softmax for rows row0 / row1
         float mx[2] = {-INFINITY, -INFINITY};
 #pragma unroll
-        for (int j = 0; j < 2; ++j) {
+        for (int sb = 0; sb < kSubPerWarp; ++sb)
 #pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            const int tok = r0 + j * 8 + tq * 2 + (e & 1);
-            const float x = tok < valid ? s[j][e] * scale_log2 : -INFINITY;
-            s[j][e] = x;
-            mx[e >> 1] = fmaxf(mx[e >> 1], x);
-          }
-        }
-        float alpha[2], m_use[2];
+          for (int j = 0; j < 2; ++j)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              const int tok = r0[sb] + j * 8 + tq * 2 + (e & 1);
+              const float x = act[sb] && tok < valid ? s[sb][j][e] * scale_log2 : -INFINITY;
+              s[sb][j][e] = x;
+              mx[e >> 1] = fmaxf(mx[e >> 1], x);
+            }
+        float m_new[2];
 #pragma unroll
         for (int h = 0; h < 2; ++h) {
           mx[h] = fmaxf(mx[h], __shfl_xor_sync(0xffffffffu, mx[h], 1));
           mx[h] = fmaxf(mx[h], __shfl_xor_sync(0xffffffffu, mx[h], 2));
-          const float m_new = fmaxf(m_r[h], mx[h]);
-          // all-masked so far: keep everything at zero weight
-          m_use[h] = m_new == -INFINITY ? 0.f : m_new;
-          alpha[h] = ex2_approx(m_r[h] - m_use[h]);
-          m_r[h] = m_new;
+          m_new[h] = fmaxf(m_r[h], mx[h]);
         }
-        float rs[2] = {0.f, 0.f};
+        // lazy rescale: only when some row's max grew by more than 2^8
+        if (__any_sync(0xffffffffu, m_new[0] > m_r[0] + kRescaleThreshold ||
+                                        m_new[1] > m_r[1] + kRescaleThreshold)) {
+          float alpha[2];
 #pragma unroll
-        for (int j = 0; j < 2; ++j) {
+          for (int h = 0; h < 2; ++h) {
+            alpha[h] = m_r[h] == -INFINITY ? 0.f : ex2_approx(m_r[h] - m_new[h]);
+            l_r[h] *= alpha[h];
+            m_r[h] = m_new[h];
+          }
 #pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            const float p = ex2_approx(s[j][e] - m_use[e >> 1]);
-            s[j][e] = p;
-            rs[e >> 1] += p;
+          for (int i = 0; i < D / 8; ++i) {
+            o_acc[i][0] *= alpha[0];
+            o_acc[i][1] *= alpha[0];
+            o_acc[i][2] *= alpha[1];
+            o_acc[i][3] *= alpha[1];
           }
         }
+        // all-masked so far: keep everything at zero weight
+        const float m_use[2] = {m_r[0] == -INFINITY ? 0.f : m_r[0],
+                                m_r[1] == -INFINITY ? 0.f : m_r[1]};
+        float rs[2] = {0.f, 0.f};
+#pragma unroll
+        for (int sb = 0; sb < kSubPerWarp; ++sb)
+#pragma unroll
+          for (int j = 0; j < 2; ++j)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              const float p = ex2_approx(s[sb][j][e] - m_use[e >> 1]);
+              s[sb][j][e] = p;
+              rs[e >> 1] += p;
+            }
 #pragma unroll
         for (int h = 0; h < 2; ++h) {
           rs[h] += __shfl_xor_sync(0xffffffffu, rs[h], 1);
           rs[h] += __shfl_xor_sync(0xffffffffu, rs[h], 2);
-          l_r[h] = l_r[h] * alpha[h] + rs[h];
-        }
-#pragma unroll
-        for (int i = 0; i < D / 8; ++i) {
-          o_acc[i][0] *= alpha[0];
-          o_acc[i][1] *= alpha[0];
-          o_acc[i][2] *= alpha[1];
-          o_acc[i][3] *= alpha[1];
+          l_r[h] += rs[h];
         }
         // P (bf16) as the A fragment of O += P V
-        uint32_t pa[4];
-        pa[0] = pack_bf16x2(s[0][0], s[0][1]);
-        pa[1] = pack_bf16x2(s[0][2], s[0][3]);
-        pa[2] = pack_bf16x2(s[1][0], s[1][1]);
-        pa[3] = pack_bf16x2(s[1][2], s[1][3]);
-        {
-          const int mi = lane >> 3;
-          const int ri = lane & 7;
-          const int tok = r0 + (mi & 1) * 8 + ri;
+        const int mi = lane >> 3;
+        const int ri = lane & 7;
+#pragma unroll
+        for (int sb = 0; sb < kSubPerWarp; ++sb) {
+          if (!act[sb]) continue;
+          uint32_t pa[4];
+          pa[0] = pack_bf16x2(s[sb][0][0], s[sb][0][1]);
+          pa[1] = pack_bf16x2(s[sb][0][2], s[sb][0][3]);
+          pa[2] = pack_bf16x2(s[sb][1][0], s[sb][1][1]);
+          pa[3] = pack_bf16x2(s[sb][1][2], s[sb][1][3]);
+          const int tok = r0[sb] + (mi & 1) * 8 + ri;
 #pragma unroll
           for (int np = 0; np < D / 16; ++np) {
             const int cg = np * 2 + (mi >> 1);
-            const uint32_t addr = vbase + (cg >> 3) * kBoxBytes + sw128(tok, cg & 7);
+            const uint32_t addr = vbase + (cg >> 3) * C::kBoxBytes + sw128(tok, cg & 7);
             uint32_t b0, b1, b2, b3;
             ldsm_x4_t(addr, b0, b1, b2, b3);
             mma16816(o_acc[np * 2], pa, b0, b1);
@@ -258,116 +362,162 @@ __global__ void __launch_bounds__(kThreads) decode_split_kernel(
           }
         }
       }
-    }
-    __syncthreads();  // every warp is done with this slot
-    if (tid == 0 && ok && !abort_flag && st + kStages < n_st) issue_stage(st + kStages);
-  }
+      // this warp is done with the slot (ldmatrix reads have completed)
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&empty_bar[slot]);
+      ++sc;
+      if (st + 1 < tg.z) continue;  // the item goes on in the next stage
 
-  if (!ok) {
-    // drain TMA copies still in flight into the ring before leaving
-    if (tid == 0) {
-      for (int st = 0; st < n_st && st < kStages; ++st) {
-        const int last = st + ((n_st - 1 - st) / kStages) * kStages;
-        mbar_drain(&full_bar[last % kStages], (last / kStages) & 1);
-      }
-      record_status(status, GQA_ERR_TIMEOUT);
-    }
-    return;
-  }
-
-  // ---- merge the warps that share an m-tile, write this split's partial
-  float* wm = reinterpret_cast<float*>(smem);            // [4][16]
-  float* wl = wm + 4 * 16;                                // [4][16]
-  float* wo = wl + 4 * 16;                                // [4][16][D]
-  if (tq == 0) {
-    wm[warp * 16 + gr] = m_r[0];
-    wm[warp * 16 + gr + 8] = m_r[1];
-    wl[warp * 16 + gr] = l_r[0];
-    wl[warp * 16 + gr + 8] = l_r[1];
-  }
+      // ---- this warp's partial for its rows and slice of the item's tokens:
+      // O / l and log2 sum-exp; a slice that saw no real token writes O = 0,
+      // lse = -inf (weight 0 in the combine)
+      {
+        const int pslot = it.split * kNSlices + slice;  // partial index within the row
 #pragma unroll
-  for (int i = 0; i < D / 8; ++i) {
-    const int col = i * 8 + tq * 2;
-    wo[(warp * 16 + gr) * D + col] = o_acc[i][0];
-    wo[(warp * 16 + gr) * D + col + 1] = o_acc[i][1];
-    wo[(warp * 16 + gr + 8) * D + col] = o_acc[i][2];
-    wo[(warp * 16 + gr + 8) * D + col + 1] = o_acc[i][3];
+        for (int h = 0; h < 2; ++h) {
+          const int row = h == 0 ? row0 : row1;
+          if (row >= Gs) continue;
+          const bool any = l_r[h] > 0.f;
+          const float inv = any ? 1.f / l_r[h] : 0.f;
+          const size_t ps = (head0 + row) * (static_cast<size_t>(n_split) * kNSlices) + pslot;
+          float* dst = part_o + ps * D + tq * 2;
+#pragma unroll
+          for (int i = 0; i < D / 8; ++i)
+            *reinterpret_cast<float2*>(dst + i * 8) =
+                make_float2(o_acc[i][2 * h] * inv, o_acc[i][2 * h + 1] * inv);
+          if (tq == 0) part_lse[ps] = any ? m_r[h] + __log2f(l_r[h]) : -INFINITY;
+        }
+      }
+    }
   }
   __syncthreads();
-  for (int idx = tid; idx < Gs * D; idx += kThreads) {
-    const int row = idx / D;
-    const int col = idx % D;
-    const int m_t = row >> 4;
-    const int r = row & 15;
-    float mc = -INFINITY;
-#pragma unroll
-    for (int sl = 0; sl < kNSlices; ++sl) mc = fmaxf(mc, wm[(sl * MT + m_t) * 16 + r]);
-    float lc = 0.f, oc = 0.f;
-#pragma unroll
-    for (int sl = 0; sl < kNSlices; ++sl) {
-      const int w = sl * MT + m_t;
-      const float ms = wm[w * 16 + r];
-      const float f = ms == -INFINITY ? 0.f : ex2_approx(ms - mc);
-      lc += f * wl[w * 16 + r];
-      oc += f * wo[(w * 16 + r) * D + col];
-    }
-    const size_t ps = (head0 + row) * n_split + split;
-    part_o[ps * D + col] = oc / lc;
-    if (col == 0) part_lse[ps] = mc + __log2f(lc);
-  }
+  if (tid == 0 && abort_flag) record_status(status, GQA_ERR_TIMEOUT);
 }
 
 // One CTA per (sequence, query head): merge the splits that hold data.
+// The weights 2^(lse_s - max) are spread over four thread groups that each
+// sum every fourth split, so the loads of many splits are in flight at once.
 template <int D>
-__global__ void __launch_bounds__(D) decode_combine_kernel(
+__global__ void __launch_bounds__(128) decode_combine_kernel(
     const float* __restrict__ part_o, const float* __restrict__ part_lse,
     const int32_t* __restrict__ seq_lens, void* __restrict__ o, int o_dtype,
-    float* __restrict__ lse_out, int h_q, int S_max, int split_len, int n_split) {
+    float* __restrict__ lse_out, int h_q, int S_max, int split_len, int n_split, int n_slices,
+    int32_t* status) {
+  constexpr int kLanesPerRow = D / 4;          // threads covering one row (float4 each)
+  constexpr int kGroups = 128 / kLanesPerRow;  // split groups
+  __shared__ float red[4];
+  __shared__ float acc_sh[kGroups][D];
   const int bh = blockIdx.x;
   const int b = bh / h_q;
-  const int col = threadIdx.x;
+  const int tid = threadIdx.x;
   int len = seq_lens[b];
-  len = len < 0 ? 0 : (len > S_max ? S_max : len);
-  const int n = (len + split_len - 1) / split_len;
-  float out = 0.f;
-  float lse_nat = -INFINITY;
-  if (n > 0) {
-    const float* pl = part_lse + static_cast<size_t>(bh) * n_split;
-    float m = -INFINITY;
-    for (int s = 0; s < n; ++s) m = fmaxf(m, pl[s]);
-    float den = 0.f, num = 0.f;
-    const float* po = part_o + static_cast<size_t>(bh) * n_split * D + col;
-    for (int s = 0; s < n; ++s) {
-      const float w = ex2_approx(pl[s] - m);
-      den += w;
-      num += w * po[static_cast<size_t>(s) * D];
+  if (len < 0 || len > S_max) {
+    if (tid == 0 && (bh % h_q) == 0) record_status(status, GQA_ERR_BAD_LENGTH);
+    len = len < 0 ? 0 : S_max;
+  }
+  // partials of this row: n_slices per split (one per token slice; a slice
+  // that saw no token holds lse = -inf and weighs nothing)
+  const int n = (len + split_len - 1) / split_len * n_slices;
+  const int n_part = n_split * n_slices;
+  const float* pl = part_lse + static_cast<size_t>(bh) * n_part;
+  // block max of the split log-sum-exps
+  float m = -INFINITY;
+  for (int s = tid; s < n; s += 128) m = fmaxf(m, pl[s]);
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, off));
+  if ((tid & 31) == 0) red[tid >> 5] = m;
+  __syncthreads();
+  m = fmaxf(fmaxf(red[0], red[1]), fmaxf(red[2], red[3]));
+  __syncthreads();
+  // block sum of the weights
+  float den = 0.f;
+  for (int s = tid; s < n; s += 128) den += ex2_approx(pl[s] - m);
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) den += __shfl_xor_sync(0xffffffffu, den, off);
+  if ((tid & 31) == 0) red[tid >> 5] = den;
+  __syncthreads();
+  den = (red[0] + red[1]) + (red[2] + red[3]);
+  // weighted sum of the partial outputs
+  const int grp = tid / kLanesPerRow;
+  const int c4 = (tid % kLanesPerRow) * 4;
+  const float* po = part_o + static_cast<size_t>(bh) * n_part * D + c4;
+  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll 4
+  for (int s = grp; s < n; s += kGroups) {
+    const float w = ex2_approx(pl[s] - m);
+    const float4 v = *reinterpret_cast<const float4*>(po + static_cast<size_t>(s) * D);
+    acc.x += w * v.x;
+    acc.y += w * v.y;
+    acc.z += w * v.z;
+    acc.w += w * v.w;
+  }
+  *reinterpret_cast<float4*>(&acc_sh[grp][c4]) = acc;
+  __syncthreads();
+  if (tid < D) {
+    float out = 0.f;
+    if (n > 0) {
+#pragma unroll
+      for (int gi = 0; gi < kGroups; ++gi) out += acc_sh[gi][tid];
+      out /= den;
     }
-    out = num / den;
-    lse_nat = (m + __log2f(den)) * 0.69314718055994531f;
+    if (o_dtype == GQA_OUT_F32)
+      static_cast<float*>(o)[static_cast<size_t>(bh) * D + tid] = out;
+    else
+      static_cast<__nv_bfloat16*>(o)[static_cast<size_t>(bh) * D + tid] =
+          __float2bfloat16_rn(out);
+    if (lse_out != nullptr && tid == 0)
+      lse_out[bh] = n > 0 ? (m + __log2f(den)) * 0.69314718055994531f : -INFINITY;
   }
-  if (o_dtype == GQA_OUT_F32) {
-    static_cast<float*>(o)[static_cast<size_t>(bh) * D + col] = out;
-  } else {
-    static_cast<__nv_bfloat16*>(o)[static_cast<size_t>(bh) * D + col] = __float2bfloat16_rn(out);
-  }
-  if (lse_out != nullptr && col == 0) lse_out[bh] = lse_nat;
 }
 
-int decode_split_len(int B, int g, int S_max) {
-  // Enough CTAs for several waves over 148 SMs while keeping each split long
-  // enough that the partial-output traffic stays small next to the K/V bytes.
-  const long long pairs = static_cast<long long>(B) * g;
-  int split = 1024;
-  while (split > kDecodeStage &&
-         pairs * ((S_max + split - 1) / split) < 148LL * 8) {
-    split /= 2;
+int decode_split_len(int B, int h_q, int g, int S_max) {
+  // Pick the split length (a multiple of the 64-token stage) that minimises
+  // the modelled time of the split pass when every sequence is full: the
+  // persistent CTAs (two per SM of a 148-SM B300) fetch items one by one, so
+  // the slowest CTA handles about ceil(items / CTAs) items of split_len
+  // tokens each, plus a fixed cost per item (query load, partial write) worth
+  // about two stages. With fewer than two items per CTA nothing can even out
+  // CTAs that stream slower than others, so such a choice pays one more item
+  // length. Only performance depends on this choice.
+  constexpr long long kSlots = 148LL * kCtasPerSm;
+  constexpr long long kItemCost = 2 * kDecodeStage;
+  const long long G = h_q / g;
+  const long long pairs = static_cast<long long>(B) * g * ((G + 31) / 32);
+  const long long s_cap = (static_cast<long long>(S_max) + kDecodeStage - 1) / kDecodeStage *
+                          kDecodeStage;
+  long long best_len = s_cap, best_cost = -1;
+  for (long long len = kDecodeStage; len <= 4096 && len < s_cap + kDecodeStage;
+       len += kDecodeStage) {
+    const long long l = len < s_cap ? len : s_cap;
+    const long long items = pairs * ((S_max + l - 1) / l);
+    const long long waves = (items + kSlots - 1) / kSlots;
+    const long long cost = waves * (l + kItemCost) + (items < 2 * kSlots ? l : 0);
+    if (best_cost < 0 || cost < best_cost) {
+      best_cost = cost;
+      best_len = l;
+    }
   }
-  return split;
+  return static_cast<int>(best_len);
 }
+
+namespace {
+
+int decode_sm_count() {
+  static int n = 0;
+  if (n == 0) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n < 1)
+      n = 148;
+  }
+  return n;
+}
+
+}  // namespace
 
 template <int D, int MT>
 static cudaError_t launch_decode_t(const DecodeArgs& a, cudaStream_t s) {
-  constexpr int kSmem = kStages * 2 * (D / 64) * kDecodeStage * 128 + 1024;
+  constexpr int kSmem = DecCfg<D>::kSmem;
   static bool attr_set = false;
   if (!attr_set) {
     cudaError_t e = cudaFuncSetAttribute(decode_split_kernel<D, MT>,
@@ -376,21 +526,28 @@ static cudaError_t launch_decode_t(const DecodeArgs& a, cudaStream_t s) {
     attr_set = true;
   }
   const int n_hslice = (a.G + 31) / 32;
-  dim3 grid(a.n_split, a.g * n_hslice, a.B);
+  const long long n_items = static_cast<long long>(a.B) * a.g * n_hslice * a.n_split;
+  const long long slots = static_cast<long long>(decode_sm_count()) * kCtasPerSm;
+  const int grid = static_cast<int>(n_items < slots ? n_items : slots);
+  // the item counter the persistent CTAs fetch from starts at zero
+  cudaError_t e = cudaMemsetAsync(a.item_counter, 0, sizeof(int), s);
+  if (e != cudaSuccess) return e;
   decode_split_kernel<D, MT><<<grid, kThreads, kSmem, s>>>(
       a.tm_k, a.tm_v, static_cast<const __nv_bfloat16*>(a.q), a.seq_lens, a.part_o, a.part_lse,
-      a.h_q, a.g, a.G, n_hslice, a.S_max, a.split_len, a.n_split, a.scale_log2, a.status);
-  cudaError_t e = cudaGetLastError();
+      a.h_q, a.g, a.G, n_hslice, a.S_max, a.split_len, a.n_split, static_cast<int>(n_items),
+      a.scale_log2, a.item_counter, a.status);
+  e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  decode_combine_kernel<D><<<a.B * a.h_q, D, 0, s>>>(a.part_o, a.part_lse, a.seq_lens, a.o,
-                                                     a.o_dtype, a.lse, a.h_q, a.S_max,
-                                                     a.split_len, a.n_split);
+  decode_combine_kernel<D><<<a.B * a.h_q, 128, 0, s>>>(a.part_o, a.part_lse, a.seq_lens, a.o,
+                                                      a.o_dtype, a.lse, a.h_q, a.S_max,
+                                                      a.split_len, a.n_split, kConsumers / MT,
+                                                      a.status);
   return cudaGetLastError();
 }
 
 cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t s) {
-  // Groups larger than 32 query heads run as 32-row slices (grid.y), each
-  // re-reading the split; no workload here has G > 32.
+  // Groups larger than 32 query heads run as 32-row slices (separate items),
+  // each re-reading the split; no workload here has G > 32.
   const int mt = (a.G + 15) / 16;
   if (a.d == 64) return mt <= 1 ? launch_decode_t<64, 1>(a, s) : launch_decode_t<64, 2>(a, s);
   return mt <= 1 ? launch_decode_t<128, 1>(a, s) : launch_decode_t<128, 2>(a, s);

@@ -23,7 +23,7 @@
 
 namespace {
 
-constexpr size_t kNoAllocScratchBytes = size_t(16) << 20;  // 16 MiB
+constexpr size_t kNoAllocScratchBytes = size_t(32) << 20;  // 32 MiB
 constexpr int kMaxDevices = 64;
 
 static __device__ __align__(256) unsigned char g_decode_scratch[kNoAllocScratchBytes];

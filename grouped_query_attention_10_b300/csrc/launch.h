@@ -15,6 +15,9 @@ constexpr int kPrefillBN = 128;
 
 // Tokens per decode pipeline stage.
 constexpr int kDecodeStage = 64;
+// Most partial results the decode split pass writes per (query head, split):
+// one per consumer warp's slice of the split's tokens.
+constexpr int kDecodeSlices = 4;
 
 struct PrefillArgs {
   CUtensorMap tm_q, tm_k, tm_v;
@@ -35,8 +38,9 @@ struct DecodeArgs {
   void* o;
   int o_dtype;
   float* lse;
-  float* part_o;    // [B, h_q, n_split, d]
-  float* part_lse;  // [B, h_q, n_split] (log2 units of the scaled scores)
+  float* part_o;    // [B, h_q, n_split * slices, d]
+  float* part_lse;  // [B, h_q, n_split * slices] (log2 units of the scaled scores)
+  int* item_counter; // work-item counter of the split pass (zeroed before each launch)
   int B, h_q, g, d, G, S_max, split_len, n_split;
   float scale_log2;
   int32_t* status;
@@ -49,6 +53,6 @@ cudaError_t launch_append(void* k_cache, void* v_cache, int32_t* seq_lens, const
                           int32_t* status, cudaStream_t s);
 
 // Split length (tokens per split-KV CTA) used for these decode sizes.
-int decode_split_len(int B, int g, int S_max);
+int decode_split_len(int B, int h_q, int g, int S_max);
 
 }  // namespace gqa

@@ -5,8 +5,10 @@
 Names: prefill_tiny, prefill_noncausal, prefill_causal, decode_ragged,
 decode_sweep_g{1,2,4,8,16,32}, append_prompt. Inputs are the seeded
 synthetic workloads of ``inputs.py``. Each timed call is bracketed by CUDA
-events on the launching stream; an L2 flush (256 MiB write) precedes every
-call. Handy for profiling one kernel in isolation.
+events on the launching stream; an L2 flush precedes every call (a 256 MiB
+write, then a 256 MiB read of another buffer, so the write's dirty lines are
+written back before the timed call starts). Handy for profiling one kernel
+in isolation.
 """
 
 from __future__ import annotations
@@ -22,6 +24,19 @@ from . import accounting, inputs
 from . import binding as gqa
 
 L2_FLUSH_BYTES = 256 << 20
+
+
+def make_l2_flush(dev):
+    """Return a function that leaves no input and no dirty line in L2 (126 MB
+    on B300): write a buffer larger than L2, then read another one."""
+    wbuf = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    rbuf = torch.ones(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+
+    def flush():
+        wbuf.fill_(1)
+        rbuf.sum()
+
+    return flush
 
 
 def _prefill(w, dev, B=None):
@@ -88,14 +103,14 @@ def main(argv=None):
     torch.cuda.set_device(dev)
     fn, work, unit, div = make(a.name, dev, a.batch)
     s = torch.cuda.current_stream(dev)
-    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    flush = make_l2_flush(dev)
     for _ in range(a.warmup):
-        flush.zero_()
+        flush()
         fn(s)
     evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
            for _ in range(a.iters)]
     for e0, e1 in evs:
-        flush.zero_()
+        flush()
         e0.record(s)
         fn(s)
         e1.record(s)

@@ -150,20 +150,21 @@ int kv_cache_append(void* k_cache, void* v_cache, int32_t* seq_lens,
  *
  * Same arguments, layouts and results as gqa_decode_fwd, minus the
  * workspace: the split-KV partials go to a scratch array built into the
- * library (gqa_decode_noalloc_scratch_bytes() bytes, 16 MiB), which every GPU
+ * library (gqa_decode_noalloc_scratch_bytes() bytes, 32 MiB), which every GPU
  * that loads the library holds until the process exits. The call allocates
  * nothing. Sizes whose gqa_decode_workspace_bytes exceeds the array are
  * rejected with GQA_ERR_SCRATCH_LIMIT before anything is queued (for
  * d = 128, h_q = 32, g = 8 the ragged B = 64, S_max = 8192 cache needs about
- * 8 MiB).
+ * 17 MiB).
  *
  *  - The first call made while a device is current looks up the array's
  *    device address on that device (cudaGetSymbolAddress) and keeps it; make
  *    that first call before any stream capture on that device.
- *  - Every call shares the one array per device. Nothing in it has to start
- *    at zero (each call writes the partials it reads), but calls that overlap
- *    on the GPU (different streams, or different host threads) race on it
- *    and give wrong results; serialise them.
+ *  - Every call shares the one array per device. The caller clears nothing:
+ *    each call writes the partials it reads and zeroes the one counter word
+ *    the split pass starts from. Calls that overlap on the GPU (different
+ *    streams, or different host threads) race on it and give wrong results;
+ *    serialise them.
  */
 int gqa_decode_fwd_noalloc(const void* q, const void* k_cache, const void* v_cache,
                            const int32_t* seq_lens, void* o, int o_dtype, float* lse, int B,
