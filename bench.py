@@ -33,6 +33,10 @@ if ROOT not in sys.path:
     sys.path.insert(0, ROOT)
 
 METRIC = "GQA prefill TFLOP/s & decode KV-read GB/s vs roofline on 1×B300"
+# DRAM bytes (read + write) of one prefill_kernel<64,false> launch of the bench workload, from
+# the ncu capture summarised in profiles/prefill_noncausal_b32_l1024_hq8_g4_d64.md; reported
+# only while prefill.cu is the source that was profiled (sha256 prefix below).
+PROFILED_PREFILL = {"sha256_prefix": "54e16f236cc6d845", "dram_bytes": 67_164_416 + 20_169_728}
 FALLBACK_PEAKS = {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0, "bf16_tflops_sustained": 1400.0}
 L2_FLUSH_BYTES = 256 << 20
 
@@ -40,7 +44,7 @@ L2_FLUSH_BYTES = 256 << 20
 def parse_args(argv=None):
     p = argparse.ArgumentParser()
     p.add_argument("--gpus", type=int, default=1)
-    p.add_argument("--steps", type=int, default=200)
+    p.add_argument("--steps", type=int, default=1000)
     p.add_argument("--warmup", type=int, default=5)
     p.add_argument("--impl", choices=["native", "reference"], default="native")
     p.add_argument("--no-extra", action="store_true", help="skip the context measurements")
@@ -318,13 +322,21 @@ def native_arm(args):
     value = units / t_max / 1e12
     ms_per_step = t_max * 1e3 / args.steps
 
+    import hashlib
+
+    src = os.path.join(ROOT, "grouped_query_attention_10_b300", "csrc", "prefill.cu")
+    with open(src, "rb") as f:
+        same_kernel = hashlib.sha256(f.read()).hexdigest().startswith(
+            PROFILED_PREFILL["sha256_prefix"])
     prefill_s = statistics.mean(prefill_ms) / 1e3
     achieved = flops_prefill / prefill_s / 1e12
     roofline = {"bound": "tensor", "kernel": "prefill_kernel<64,false>",
                 "achieved": round(achieved, 2), "peak": peaks["bf16_tflops"],
                 "unit": "TFLOP/s", "frac": round(achieved / peaks["bf16_tflops"], 4),
                 "peak_source": f"{peak_src} bf16 dense burst",
-                "traffic": None}
+                "traffic": PROFILED_PREFILL["dram_bytes"] if same_kernel else None,
+                "traffic_unit": "bytes per launch (ncu dram read+write)",
+                "algorithmic_bytes": accounting.prefill_bytes(B, L, h_q, g, d, 4)}
 
     # ---- end to end: pinned host inputs in, results back, copies timed
     pin = lambda t: t.detach().to("cpu").pin_memory()

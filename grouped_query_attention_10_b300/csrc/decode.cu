@@ -394,18 +394,25 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) decode_split_kernel(
   if (tid == 0 && abort_flag) record_status(status, GQA_ERR_TIMEOUT);
 }
 
-// One CTA per (sequence, query head): merge the splits that hold data.
-// The weights 2^(lse_s - max) are spread over four thread groups that each
-// sum every fourth split, so the loads of many splits are in flight at once.
+// One CTA per (sequence, query head): merge the partials that hold data.
+// The log2 sum-exps are staged in shared memory (up to kCombineSmem of
+// them; longer rows loop over global memory), the weights 2^(lse - max) are
+// computed once, and eight thread groups each sum every eighth partial of
+// float4 columns, so many partial loads are in flight at once.
+constexpr int kCombineThreads = 256;
+constexpr int kCombineSmem = 2048;
+
 template <int D>
-__global__ void __launch_bounds__(128) decode_combine_kernel(
+__global__ void __launch_bounds__(kCombineThreads) decode_combine_kernel(
     const float* __restrict__ part_o, const float* __restrict__ part_lse,
     const int32_t* __restrict__ seq_lens, void* __restrict__ o, int o_dtype,
     float* __restrict__ lse_out, int h_q, int S_max, int split_len, int n_split, int n_slices,
     int32_t* status) {
-  constexpr int kLanesPerRow = D / 4;          // threads covering one row (float4 each)
-  constexpr int kGroups = 128 / kLanesPerRow;  // split groups
-  __shared__ float red[4];
+  constexpr int kLanesPerRow = D / 4;                       // threads covering one row
+  constexpr int kGroups = kCombineThreads / kLanesPerRow;   // partial groups
+  constexpr int kWarps = kCombineThreads / 32;
+  __shared__ float red[kWarps];
+  __shared__ float wsh[kCombineSmem];
   __shared__ float acc_sh[kGroups][D];
   const int bh = blockIdx.x;
   const int b = bh / h_q;
@@ -420,23 +427,37 @@ __global__ void __launch_bounds__(128) decode_combine_kernel(
   const int n = (len + split_len - 1) / split_len * n_slices;
   const int n_part = n_split * n_slices;
   const float* pl = part_lse + static_cast<size_t>(bh) * n_part;
-  // block max of the split log-sum-exps
+  const bool staged = n <= kCombineSmem;
+  auto lse_at = [&](int s) { return staged ? wsh[s] : pl[s]; };
+  // block max of the partial log-sum-exps
   float m = -INFINITY;
-  for (int s = tid; s < n; s += 128) m = fmaxf(m, pl[s]);
+  for (int s = tid; s < n; s += kCombineThreads) {
+    const float x = pl[s];
+    if (staged) wsh[s] = x;
+    m = fmaxf(m, x);
+  }
 #pragma unroll
   for (int off = 16; off > 0; off >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, off));
   if ((tid & 31) == 0) red[tid >> 5] = m;
   __syncthreads();
-  m = fmaxf(fmaxf(red[0], red[1]), fmaxf(red[2], red[3]));
+  m = red[0];
+#pragma unroll
+  for (int w = 1; w < kWarps; ++w) m = fmaxf(m, red[w]);
   __syncthreads();
-  // block sum of the weights
+  // weights (kept in shared memory when staged) and their block sum
   float den = 0.f;
-  for (int s = tid; s < n; s += 128) den += ex2_approx(pl[s] - m);
+  for (int s = tid; s < n; s += kCombineThreads) {
+    const float w = ex2_approx(lse_at(s) - m);
+    if (staged) wsh[s] = w;
+    den += w;
+  }
 #pragma unroll
   for (int off = 16; off > 0; off >>= 1) den += __shfl_xor_sync(0xffffffffu, den, off);
   if ((tid & 31) == 0) red[tid >> 5] = den;
   __syncthreads();
-  den = (red[0] + red[1]) + (red[2] + red[3]);
+  den = 0.f;
+#pragma unroll
+  for (int w = 0; w < kWarps; ++w) den += red[w];
   // weighted sum of the partial outputs
   const int grp = tid / kLanesPerRow;
   const int c4 = (tid % kLanesPerRow) * 4;
@@ -444,7 +465,7 @@ __global__ void __launch_bounds__(128) decode_combine_kernel(
   float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll 4
   for (int s = grp; s < n; s += kGroups) {
-    const float w = ex2_approx(pl[s] - m);
+    const float w = staged ? wsh[s] : ex2_approx(pl[s] - m);
     const float4 v = *reinterpret_cast<const float4*>(po + static_cast<size_t>(s) * D);
     acc.x += w * v.x;
     acc.y += w * v.y;
@@ -538,7 +559,7 @@ static cudaError_t launch_decode_t(const DecodeArgs& a, cudaStream_t s) {
       a.scale_log2, a.item_counter, a.status);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  decode_combine_kernel<D><<<a.B * a.h_q, 128, 0, s>>>(a.part_o, a.part_lse, a.seq_lens, a.o,
+  decode_combine_kernel<D><<<a.B * a.h_q, kCombineThreads, 0, s>>>(a.part_o, a.part_lse, a.seq_lens, a.o,
                                                       a.o_dtype, a.lse, a.h_q, a.S_max,
                                                       a.split_len, a.n_split, kConsumers / MT,
                                                       a.status);
