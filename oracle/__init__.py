@@ -13,6 +13,7 @@ from .gqa_oracle import (  # noqa: F401
     head_map,
     attention_probs,
     prefill,
+    prefill_cached,
     decode,
     append,
 )

@@ -23,9 +23,23 @@ What it computes, and where the pages define it
   Attention" explainer (ijyty.com), section 2.1 and section 2.2 (second step),
   section 3.2 (cache concat).
 
+* Score-bias variants named by the pages: the sliding-window attention of
+  Mistral (the model table of the zeeklog.com page, section 2.4) and ALiBi,
+  a per-head linear distance penalty ``-slope_h * |i - j|`` added to the
+  scores (the jsqmd.com survey, section 3.2).
+* Chunked prefill against a KV cache: new query tokens attend to the cached
+  rows and, causally, to each other (the cache concatenation of the ijyty.com
+  explainer, section 3.2, applied to more than one new token).
+
 Readings where the pages are silent (each listed in the design notes):
 * causal mask: key ``j`` is visible to query ``i`` iff ``j <= i + q_offset``
-  (``q_offset = 0`` when queries and keys cover the same positions);
+  (``q_offset = 0`` when queries and keys cover the same positions; a chunk
+  of T new tokens over L cached keys has ``q_offset = L - T``);
+* sliding window of size W (causal only): key ``j`` is also required to
+  satisfy ``j > i + q_offset - W``;
+* ALiBi: ``slope_h * |i + q_offset - j|`` (natural-log units, one slope per
+  query head, supplied by the caller) is subtracted from the scaled score;
+* a decode query sits at position ``seq_len - 1`` of its sequence;
 * dropout is the identity (inference);
 * a decode row with zero valid cache rows returns zeros and ``lse = -inf``;
 * ``append`` drops rows that would land past ``S_max`` and reports it.
@@ -95,9 +109,18 @@ def _expand_kv(x: np.ndarray, group_size: int, axis: int) -> np.ndarray:
     return np.repeat(x, group_size, axis=axis)
 
 
-def _visible(i: int, j: int, q_offset: int) -> bool:
-    """Causal visibility of key ``j`` to query row ``i``."""
-    return j <= i + q_offset
+def _visible(i: int, j: int, q_offset: int, window: int = 0) -> bool:
+    """Causal visibility of key ``j`` to query row ``i`` (and the window)."""
+    if j > i + q_offset:
+        return False
+    return window <= 0 or j > i + q_offset - window
+
+
+def _alibi_bias(n_q: int, n_k: int, slope: float, q_offset: int) -> np.ndarray:
+    """ALiBi penalty ``-slope * |i + q_offset - j|`` for every (query, key)."""
+    i = np.arange(n_q)[:, None] + q_offset
+    j = np.arange(n_k)[None, :]
+    return -slope * np.abs(i - j).astype(np.float64)
 
 
 def _softmax_rows(scores: np.ndarray):
@@ -147,14 +170,20 @@ def attention_probs(q, k, causal: bool, scale: float, q_offset: int = 0):
     return out
 
 
-def prefill(q, k, v, causal: bool, scale: float, q_offset: int = 0):
-    """GQA prefill: ``O = softmax(Q K_rep^T * scale + mask) V_rep``.
+def prefill(q, k, v, causal: bool, scale: float, q_offset: int = 0, window: int = 0,
+            alibi_slopes=None):
+    """GQA prefill: ``O = softmax(Q K_rep^T * scale + bias + mask) V_rep``.
 
     q: [B, Lq, h_q, d]; k, v: [B, Lk, g, d] (the projection output layout
     ``view(B, L, heads, d_head)``).  Returns (O [B, Lq, h_q, d] fp64,
-    lse [B, h_q, Lq] fp64, natural log).  With ``causal`` the query row ``i``
-    sits at key position ``i + q_offset``.
+    lse [B, h_q, Lq] fp64, natural log).  Query row ``i`` sits at key
+    position ``i + q_offset``; ``causal`` hides later keys, ``window`` > 0
+    (causal only) also hides keys ``window`` or more positions back, and
+    ``alibi_slopes`` ([h_q], or None) subtracts ``slope_h * distance``.
+    A row that sees no key returns zeros and lse = -inf.
     """
+    if window > 0 and not causal:
+        raise ValueError("a sliding window needs causal attention")
     q = np.asarray(q, dtype=np.float64)
     k = np.asarray(k, dtype=np.float64)
     v = np.asarray(v, dtype=np.float64)
@@ -167,7 +196,7 @@ def prefill(q, k, v, causal: bool, scale: float, q_offset: int = 0):
         mask = np.zeros((Lq, Lk), dtype=bool)
         for i in range(Lq):
             for j in range(Lk):
-                mask[i, j] = not _visible(i, j, q_offset)
+                mask[i, j] = not _visible(i, j, q_offset, window)
     out = np.empty((B, Lq, h_q, d))
     lse = np.empty((B, h_q, Lq))
     for b in range(B):
@@ -176,6 +205,8 @@ def prefill(q, k, v, causal: bool, scale: float, q_offset: int = 0):
         v_rep = _expand_kv(v[b], group_size, axis=1)
         for h in range(h_q):
             s = (q[b, :, h, :] @ k_rep[:, h, :].T) * scale
+            if alibi_slopes is not None:
+                s = s + _alibi_bias(Lq, Lk, float(alibi_slopes[h]), q_offset)
             if causal:
                 s[mask] = -np.inf
             p, m, ssum = _softmax_rows(s)
@@ -184,16 +215,46 @@ def prefill(q, k, v, causal: bool, scale: float, q_offset: int = 0):
     return out, lse
 
 
+def prefill_cached(q, k_cache, v_cache, seq_lens, scale: float, window: int = 0,
+                   alibi_slopes=None):
+    """Chunked prefill over a KV cache (bottom-right causal alignment).
+
+    q: [B, T, h_q, d], the T newest tokens of each sequence; k_cache,
+    v_cache: [B, g, S_max, d] already holding those tokens' K/V at the end of
+    each sequence; seq_lens: [B] rows per sequence, each >= T. Token ``t`` of
+    sequence ``b`` sits at position ``seq_lens[b] - T + t`` and sees every
+    cached row up to its own position. Returns (O [B, T, h_q, d],
+    lse [B, h_q, T]).
+    """
+    q = np.asarray(q, dtype=np.float64)
+    B, T = q.shape[0], q.shape[1]
+    outs, lses = [], []
+    for b in range(B):
+        n = int(seq_lens[b])
+        if n < T:
+            raise ValueError("every sequence must hold at least the T new tokens")
+        # the cache rows of this sequence in the projection layout [1, n, g, d]
+        kb = np.asarray(k_cache[b:b + 1, :, :n, :], dtype=np.float64).transpose(0, 2, 1, 3)
+        vb = np.asarray(v_cache[b:b + 1, :, :n, :], dtype=np.float64).transpose(0, 2, 1, 3)
+        o, l = prefill(q[b:b + 1], kb, vb, True, scale, q_offset=n - T, window=window,
+                       alibi_slopes=alibi_slopes)
+        outs.append(o)
+        lses.append(l)
+    return np.concatenate(outs, axis=0), np.concatenate(lses, axis=0)
+
+
 # ---------------------------------------------------------------------------
 # Decode over a [B, g, S_max, d] KV cache
 # ---------------------------------------------------------------------------
 
-def decode(q, k_cache, v_cache, seq_lens, scale: float):
+def decode(q, k_cache, v_cache, seq_lens, scale: float, window: int = 0, alibi_slopes=None):
     """One-token GQA decode over the cache.
 
     q: [B, h_q, d]; k_cache, v_cache: [B, g, S_max, d]; seq_lens: [B] valid
-    rows per sequence. Row ``j`` of sequence ``b`` is visible iff
-    ``j < seq_lens[b]``. Returns (O [B, h_q, d], lse [B, h_q]).
+    rows per sequence. The query sits at position ``seq_lens[b] - 1``; row
+    ``j`` of sequence ``b`` is visible iff ``j < seq_lens[b]`` (and, with a
+    window, ``j >= seq_lens[b] - window``); ``alibi_slopes`` subtracts
+    ``slope_h * (seq_lens[b] - 1 - j)``. Returns (O [B, h_q, d], lse [B, h_q]).
     """
     q = np.asarray(q, dtype=np.float64)
     k_cache = np.asarray(k_cache, dtype=np.float64)
@@ -211,6 +272,10 @@ def decode(q, k_cache, v_cache, seq_lens, scale: float):
         v_rep = _expand_kv(v_cache[b, :, :n, :], group_size, axis=0)
         for h in range(h_q):
             s = (k_rep[h] @ q[b, h]) * scale  # [n]
+            if alibi_slopes is not None:
+                s = s + _alibi_bias(1, n, float(alibi_slopes[h]), n - 1)[0]
+            if window > 0:
+                s = np.where(np.arange(n) >= n - window, s, -np.inf)
             p, m, ssum = _softmax_rows(s[None, :])
             out[b, h] = (p @ v_rep[h])[0]
             lse[b, h] = _lse(m, ssum)[0, 0]

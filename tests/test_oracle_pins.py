@@ -121,10 +121,67 @@ def check_causal_row0_is_v0():
         assert np.array_equal(o[:, 0, h, :], v[:, 0, h // 4, :])
 
 
+def _band_mask(Lq, Lk, q_offset, window):
+    """Boolean visibility built with torch primitives (True = visible)."""
+    i = torch.arange(Lq)[:, None] + q_offset
+    j = torch.arange(Lk)[None, :]
+    vis = j <= i
+    if window > 0:
+        vis = vis & (j > i - window)
+    return vis
+
+
+def check_window_against_sdpa_mask():
+    for (B, L, h_q, g, d, W, seed) in [(2, 11, 8, 2, 8, 3, 41), (1, 9, 4, 4, 16, 1, 42),
+                                       (1, 12, 8, 1, 8, 5, 43)]:
+        q = _rand((B, L, h_q, d), seed)
+        k = _rand((B, L, g, d), seed + 1)
+        v = _rand((B, L, g, d), seed + 2)
+        scale = 1.0 / math.sqrt(d)
+        o, _ = oracle.prefill(q, k, v, True, scale, window=W)
+        tq, tk, tv = (torch.from_numpy(x).transpose(1, 2) for x in (q, k, v))
+        ref = F.scaled_dot_product_attention(tq, tk, tv, attn_mask=_band_mask(L, L, 0, W),
+                                             scale=scale, enable_gqa=True)
+        np.testing.assert_allclose(o, ref.transpose(1, 2).numpy(), rtol=0, atol=1e-12)
+
+
+def check_window_one_returns_own_v():
+    q = _rand((2, 6, 8, 8), 51)
+    k = _rand((2, 6, 2, 8), 52)
+    v = _rand((2, 6, 2, 8), 53)
+    o, _ = oracle.prefill(q, k, v, True, 0.4, window=1)
+    for h in range(8):
+        assert np.array_equal(o[:, :, h, :], v[:, :, h // 4, :])
+
+
+def check_alibi_causal_against_sdpa_augmented():
+    # causal ALiBi: -slope*(i - j) = slope*j - slope*i, and the per-row term
+    # cancels in the softmax; so it equals plain attention on per-head
+    # vectors augmented with one coordinate: q' = [q, 1], k'_j = [k_j, slope*j/scale]
+    B, L, h_q, g, d = 2, 10, 8, 2, 8
+    q = _rand((B, L, h_q, d), 61)
+    k = _rand((B, L, g, d), 62)
+    v = _rand((B, L, g, d), 63)
+    slopes = np.array([2.0 ** (-8.0 * (h + 1) / h_q) for h in range(h_q)])
+    scale = 1.0 / math.sqrt(d)
+    o, _ = oracle.prefill(q, k, v, True, scale, alibi_slopes=slopes)
+    G = h_q // g
+    tq = torch.from_numpy(q).transpose(1, 2)                       # [B, h_q, L, d]
+    tk = torch.from_numpy(k).transpose(1, 2).repeat_interleave(G, dim=1)
+    tv = torch.from_numpy(v).transpose(1, 2).repeat_interleave(G, dim=1)
+    pos = torch.arange(L, dtype=torch.float64)
+    extra_k = torch.from_numpy(slopes)[:, None] * pos[None, :] / scale  # [h_q, L]
+    qa = torch.cat([tq, torch.ones(B, h_q, L, 1, dtype=torch.float64)], dim=-1)
+    ka = torch.cat([tk, extra_k[None, :, :, None].expand(B, h_q, L, 1)], dim=-1)
+    ref = F.scaled_dot_product_attention(qa, ka, tv, is_causal=True, scale=scale)
+    np.testing.assert_allclose(o, ref.transpose(1, 2).numpy(), rtol=0, atol=1e-10)
+
+
 def _all_checks():
     return [check_golden_prefill, check_golden_decode, check_against_sdpa,
             check_permutation_within_group, check_rows_sum_to_one,
-            check_causal_row0_is_v0]
+            check_causal_row0_is_v0, check_window_against_sdpa_mask,
+            check_window_one_returns_own_v, check_alibi_causal_against_sdpa_augmented]
 
 
 # ---------------------------------------------------------------------------
@@ -342,7 +399,13 @@ def _softmax_wrong_axis(scores):
 
 MUTANTS = {
     "modulo_head_map": ("_expand_kv", _tile_heads),
-    "causal_off_by_one": ("_visible", lambda i, j, off: j < i + off),
+    "causal_off_by_one": ("_visible", lambda i, j, off, window=0: j < i + off),
+    "window_off_by_one": ("_visible",
+                          lambda i, j, off, window=0: j <= i + off and
+                          (window <= 0 or j >= i + off - window)),
+    "alibi_wrong_sign": ("_alibi_bias",
+                         lambda n_q, n_k, slope, off: slope * np.abs(
+                             np.arange(n_q)[:, None] + off - np.arange(n_k)[None, :])),
     "softmax_wrong_axis": ("_softmax_rows", _softmax_wrong_axis),
     "lse_without_max": ("_lse", lambda m, s: np.log(s)),
 }
@@ -359,3 +422,113 @@ def test_planted_mistake_is_caught(name, monkeypatch):
         except (AssertionError, ValueError, IndexError):
             caught += 1
     assert caught >= 1, f"mutant {name} passed every pin"
+
+
+# ---------------------------------------------------------------------------
+# Score-bias variants and chunked prefill over a cache
+# ---------------------------------------------------------------------------
+
+def test_window_matches_library_sdpa_with_band_mask():
+    check_window_against_sdpa_mask()
+
+
+def test_window_one_returns_own_v_exactly():
+    check_window_one_returns_own_v()
+
+
+def test_window_at_least_the_length_is_plain_causal():
+    q, k, v = _rand((1, 7, 4, 8), 71), _rand((1, 7, 2, 8), 72), _rand((1, 7, 2, 8), 73)
+    o_w, l_w = oracle.prefill(q, k, v, True, 0.3, window=7)
+    o, l = oracle.prefill(q, k, v, True, 0.3)
+    np.testing.assert_array_equal(o_w, o)
+    np.testing.assert_array_equal(l_w, l)
+
+
+def test_window_requires_causal():
+    q, k = _rand((1, 3, 2, 4), 74), _rand((1, 3, 1, 4), 75)
+    with pytest.raises(ValueError):
+        oracle.prefill(q, k, k, False, 0.5, window=2)
+
+
+def test_alibi_causal_matches_library_sdpa_on_augmented_vectors():
+    check_alibi_causal_against_sdpa_augmented()
+
+
+def test_alibi_zero_slopes_is_plain_attention():
+    q, k, v = _rand((2, 6, 4, 8), 81), _rand((2, 6, 2, 8), 82), _rand((2, 6, 2, 8), 83)
+    for causal in (True, False):
+        o_a, l_a = oracle.prefill(q, k, v, causal, 0.3, alibi_slopes=np.zeros(4))
+        o, l = oracle.prefill(q, k, v, causal, 0.3)
+        np.testing.assert_allclose(o_a, o, rtol=0, atol=1e-15)
+        np.testing.assert_allclose(l_a, l, rtol=0, atol=1e-15)
+
+
+def test_alibi_noncausal_brute_force_loops():
+    B, L, h_q, g, d = 1, 4, 4, 2, 3
+    q, k, v = _rand((B, L, h_q, d), 91), _rand((B, L, g, d), 92), _rand((B, L, g, d), 93)
+    slopes = [0.5, 0.25, 0.125, 0.0625]
+    scale = 0.7
+    o, lse = oracle.prefill(q, k, v, False, scale, alibi_slopes=np.array(slopes))
+    for h in range(h_q):
+        kv = h // (h_q // g)
+        for i in range(L):
+            w = [math.exp(scale * sum(q[0, i, h, c] * k[0, j, kv, c] for c in range(d))
+                          - slopes[h] * abs(i - j)) for j in range(L)]
+            tot = sum(w)
+            for c in range(d):
+                ref = sum(w[j] * v[0, j, kv, c] for j in range(L)) / tot
+                assert abs(o[0, i, h, c] - ref) < 1e-12
+            assert abs(lse[0, h, i] - math.log(tot)) < 1e-12
+
+
+def test_prefill_cached_equals_tail_of_full_causal_prefill():
+    B, T, h_q, g, d, S_max = 3, 4, 8, 2, 8, 13
+    lens = [9, 4, 13]
+    rng_seed = 101
+    for window, alibi in ((0, None), (3, None), (0, [2.0 ** -(h + 1) for h in range(h_q)]),
+                          (5, [0.3] * h_q)):
+        kc, vc = _rand((B, g, S_max, d), rng_seed), _rand((B, g, S_max, d), rng_seed + 1)
+        q_full = _rand((B, S_max, h_q, d), rng_seed + 2)
+        q_new = np.stack([q_full[b, lens[b] - T:lens[b]] for b in range(B)])
+        slopes = None if alibi is None else np.array(alibi)
+        o, lse = oracle.prefill_cached(q_new, kc, vc, lens, 0.35, window=window,
+                                       alibi_slopes=slopes)
+        for b in range(B):
+            n = lens[b]
+            k_full = kc[b:b + 1, :, :n].transpose(0, 2, 1, 3)
+            v_full = vc[b:b + 1, :, :n].transpose(0, 2, 1, 3)
+            o_f, l_f = oracle.prefill(q_full[b:b + 1, :n], k_full, v_full, True, 0.35,
+                                      window=window, alibi_slopes=slopes)
+            np.testing.assert_allclose(o[b], o_f[0, n - T:], rtol=0, atol=1e-12)
+            np.testing.assert_allclose(lse[b], l_f[0, :, n - T:], rtol=0, atol=1e-12)
+
+
+def test_decode_with_window_and_alibi_is_one_token_chunk():
+    B, h_q, g, d, S_max = 3, 8, 4, 8, 12
+    kc, vc = _rand((B, g, S_max, d), 111), _rand((B, g, S_max, d), 112)
+    q = _rand((B, h_q, d), 113)
+    lens = [12, 5, 1]
+    slopes = np.array([2.0 ** (-8.0 * (h + 1) / h_q) for h in range(h_q)])
+    for window in (0, 1, 4):
+        for al in (None, slopes):
+            o, lse = oracle.decode(q, kc, vc, lens, 0.4, window=window, alibi_slopes=al)
+            o_c, l_c = oracle.prefill_cached(q[:, None], kc, vc, lens, 0.4, window=window,
+                                             alibi_slopes=al)
+            np.testing.assert_allclose(o, o_c[:, 0], rtol=0, atol=1e-12)
+            np.testing.assert_allclose(lse, l_c[:, :, 0], rtol=0, atol=1e-12)
+
+
+def test_decode_window_equals_decode_over_the_last_rows():
+    # ALiBi depends on distance only, so moving the window's rows to the
+    # front of a shorter cache leaves the result unchanged
+    B, h_q, g, d, S_max, W = 2, 4, 2, 8, 10, 3
+    kc, vc = _rand((B, g, S_max, d), 121), _rand((B, g, S_max, d), 122)
+    q = _rand((B, h_q, d), 123)
+    lens = [10, 7]
+    slopes = np.array([0.5, 0.25, 0.125, 0.0625])
+    o, _ = oracle.decode(q, kc, vc, lens, 0.5, window=W, alibi_slopes=slopes)
+    for b in range(B):
+        n = lens[b]
+        o_t, _ = oracle.decode(q[b:b + 1], kc[b:b + 1, :, n - W:n], vc[b:b + 1, :, n - W:n],
+                               [W], 0.5, alibi_slopes=slopes)
+        np.testing.assert_allclose(o[b], o_t[0], rtol=0, atol=1e-12)
