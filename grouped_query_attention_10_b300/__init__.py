@@ -11,6 +11,7 @@ from .binding import (  # noqa: F401
     gqa_decode_fwd,
     gqa_decode_workspace_bytes,
     gqa_prefill_fwd,
+    gqa_prefill_kvcache_fwd,
     gqa_status_string,
     kv_cache_append,
     load_library,

@@ -58,6 +58,15 @@ def load_library() -> ctypes.CDLL:
     lib.gqa_prefill_fwd.argtypes = [vp, vp, vp, vp, i32, vp, i32, i32, i32, i32, i32, f32,
                                     i32, vp, vp]
     lib.gqa_prefill_fwd.restype = i32
+    lib.gqa_prefill_fwd_ex.argtypes = [vp, vp, vp, vp, i32, vp, i32, i32, i32, i32, i32, f32,
+                                       i32, i32, vp, vp, vp]
+    lib.gqa_prefill_fwd_ex.restype = i32
+    lib.gqa_prefill_kvcache_fwd.argtypes = [vp, vp, vp, vp, vp, i32, vp, i32, i32, i32, i32,
+                                            i32, i32, f32, i32, vp, vp, vp]
+    lib.gqa_prefill_kvcache_fwd.restype = i32
+    lib.gqa_decode_fwd_ex.argtypes = [vp, vp, vp, vp, vp, i32, vp, i32, i32, i32, i32, i32, f32,
+                                      i32, vp, vp, sz, vp, vp]
+    lib.gqa_decode_fwd_ex.restype = i32
     lib.gqa_decode_workspace_bytes.argtypes = [i32, i32, i32, i32, i32]
     lib.gqa_decode_workspace_bytes.restype = sz
     lib.gqa_decode_fwd.argtypes = [vp, vp, vp, vp, vp, i32, vp, i32, i32, i32, i32, i32, f32,
@@ -112,11 +121,20 @@ def _out_code(dtype) -> int:
     raise TypeError("output dtype must be float32 or bfloat16")
 
 
+def _check_slopes(alibi_slopes, h_q):
+    if alibi_slopes is not None:
+        _check(alibi_slopes, "alibi_slopes", torch.float32, (h_q,))
+
+
 def gqa_prefill_fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, *, causal: bool,
                     scale: Optional[float] = None, out: Optional[torch.Tensor] = None,
                     out_dtype=torch.float32, lse: Optional[torch.Tensor] = None,
-                    status: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
-    """Prefill attention. q [B,L,h_q,d], k/v [B,L,g,d] bf16 -> out [B,L,h_q,d]."""
+                    status: Optional[torch.Tensor] = None, stream=None, window: int = 0,
+                    alibi_slopes: Optional[torch.Tensor] = None) -> torch.Tensor:
+    """Prefill attention. q [B,L,h_q,d], k/v [B,L,g,d] bf16 -> out [B,L,h_q,d].
+
+    ``window`` > 0 (causal only) keeps the last ``window`` keys of every row;
+    ``alibi_slopes`` (fp32 [h_q]) subtracts ``slope_h * |i - j|``."""
     lib = load_library()
     B, L, h_q, d = q.shape
     g = k.shape[2]
@@ -130,13 +148,54 @@ def gqa_prefill_fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, *, causal
         _check(lse, "lse", torch.float32, (B, h_q, L))
     if status is not None:
         _check(status, "status", torch.int32)
+    _check_slopes(alibi_slopes, h_q)
     if scale is None:
         scale = 1.0 / (d ** 0.5)
-    rc = lib.gqa_prefill_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _out_code(out.dtype),
-                             _ptr(lse), B, L, h_q, g, d, float(scale), int(bool(causal)),
-                             _ptr(status), _stream_ptr(stream, q.device))
+    if window == 0 and alibi_slopes is None:
+        rc = lib.gqa_prefill_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _out_code(out.dtype),
+                                 _ptr(lse), B, L, h_q, g, d, float(scale), int(bool(causal)),
+                                 _ptr(status), _stream_ptr(stream, q.device))
+    else:
+        rc = lib.gqa_prefill_fwd_ex(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _out_code(out.dtype),
+                                    _ptr(lse), B, L, h_q, g, d, float(scale),
+                                    int(bool(causal)), int(window), _ptr(alibi_slopes),
+                                    _ptr(status), _stream_ptr(stream, q.device))
     if rc != GQA_OK:
         raise GQAError(rc, "gqa_prefill_fwd")
+    return out
+
+
+def gqa_prefill_kvcache_fwd(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor,
+                            seq_lens: torch.Tensor, *, scale: Optional[float] = None,
+                            out: Optional[torch.Tensor] = None, out_dtype=torch.float32,
+                            lse: Optional[torch.Tensor] = None, window: int = 0,
+                            alibi_slopes: Optional[torch.Tensor] = None,
+                            status: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
+    """Chunked prefill: q [B,T,h_q,d] (the T newest tokens) over a [B,g,S_max,d]
+    cache that already holds them; seq_lens [B] device int32, each >= T."""
+    lib = load_library()
+    B, T, h_q, d = q.shape
+    g, S_max = k_cache.shape[1], k_cache.shape[2]
+    _check(q, "q", torch.bfloat16)
+    _check(k_cache, "k_cache", torch.bfloat16, (B, g, S_max, d))
+    _check(v_cache, "v_cache", torch.bfloat16, (B, g, S_max, d))
+    _check(seq_lens, "seq_lens", torch.int32, (B,))
+    if out is None:
+        out = torch.empty((B, T, h_q, d), dtype=out_dtype, device=q.device)
+    _check(out, "out", out.dtype, (B, T, h_q, d))
+    if lse is not None:
+        _check(lse, "lse", torch.float32, (B, h_q, T))
+    if status is not None:
+        _check(status, "status", torch.int32)
+    _check_slopes(alibi_slopes, h_q)
+    if scale is None:
+        scale = 1.0 / (d ** 0.5)
+    rc = lib.gqa_prefill_kvcache_fwd(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(seq_lens),
+                                     _ptr(out), _out_code(out.dtype), _ptr(lse), B, T, h_q, g,
+                                     d, S_max, float(scale), int(window), _ptr(alibi_slopes),
+                                     _ptr(status), _stream_ptr(stream, q.device))
+    if rc != GQA_OK:
+        raise GQAError(rc, "gqa_prefill_kvcache_fwd")
     return out
 
 
@@ -149,8 +208,12 @@ def gqa_decode_fwd(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor
                    out: Optional[torch.Tensor] = None, out_dtype=torch.float32,
                    lse: Optional[torch.Tensor] = None,
                    workspace: Optional[torch.Tensor] = None,
-                   status: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
-    """Decode one token per sequence over a [B,g,S_max,d] cache -> out [B,h_q,d]."""
+                   status: Optional[torch.Tensor] = None, stream=None, window: int = 0,
+                   alibi_slopes: Optional[torch.Tensor] = None) -> torch.Tensor:
+    """Decode one token per sequence over a [B,g,S_max,d] cache -> out [B,h_q,d].
+
+    ``window`` > 0 keeps the last ``window`` rows; ``alibi_slopes`` (fp32 [h_q])
+    subtracts ``slope_h * (seq_lens[b] - 1 - j)``."""
     lib = load_library()
     B, h_q, d = q.shape
     g, S_max = k_cache.shape[1], k_cache.shape[2]
@@ -171,10 +234,18 @@ def gqa_decode_fwd(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor
     _check(workspace, "workspace", torch.uint8)
     if scale is None:
         scale = 1.0 / (d ** 0.5)
-    rc = lib.gqa_decode_fwd(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(seq_lens), _ptr(out),
-                            _out_code(out.dtype), _ptr(lse), B, h_q, g, d, S_max, float(scale),
-                            _ptr(workspace), workspace.numel(), _ptr(status),
-                            _stream_ptr(stream, q.device))
+    _check_slopes(alibi_slopes, h_q)
+    if window == 0 and alibi_slopes is None:
+        rc = lib.gqa_decode_fwd(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(seq_lens),
+                                _ptr(out), _out_code(out.dtype), _ptr(lse), B, h_q, g, d, S_max,
+                                float(scale), _ptr(workspace), workspace.numel(), _ptr(status),
+                                _stream_ptr(stream, q.device))
+    else:
+        rc = lib.gqa_decode_fwd_ex(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(seq_lens),
+                                   _ptr(out), _out_code(out.dtype), _ptr(lse), B, h_q, g, d,
+                                   S_max, float(scale), int(window), _ptr(alibi_slopes),
+                                   _ptr(workspace), workspace.numel(), _ptr(status),
+                                   _stream_ptr(stream, q.device))
     if rc != GQA_OK:
         raise GQAError(rc, "gqa_decode_fwd")
     return out

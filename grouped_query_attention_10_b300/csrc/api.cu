@@ -121,21 +121,35 @@ const char* gqa_status_string(int status) {
 
 int gqa_version(void) { return 100; }
 
-int gqa_prefill_fwd(const void* q, const void* k, const void* v, void* o, int o_dtype,
-                    float* lse, int B, int L, int h_q, int g, int d, float scale, int causal,
-                    int32_t* status_dev, void* stream) {
+}  // extern "C"
+
+namespace {
+
+// Shared by the prefill entry points. K/V come either in the projection
+// layout [B, Lk, g, d] (kv_lens == nullptr, Lk == Lq) or from a cache
+// [B, g, S_max, d] with per-sequence key counts kv_lens (then kv_extent is
+// S_max and the queries are the last Lq keys of every sequence).
+int prefill_common(const void* q, const void* k, const void* v, const int32_t* kv_lens, void* o,
+                   int o_dtype, float* lse, int B, int Lq, int kv_extent, int h_q, int g, int d,
+                   float scale, int causal, int window, const float* alibi, int32_t* status_dev,
+                   void* stream) {
   if (q == nullptr || k == nullptr || v == nullptr || o == nullptr) return GQA_ERR_NULL;
-  if (B < 1 || B > 65535 || L < 1 || !heads_ok(h_q, g, d) || g > 65535) return GQA_ERR_SHAPE;
+  if (B < 1 || B > 65535 || Lq < 1 || kv_extent < 1 || !heads_ok(h_q, g, d) || g > 65535)
+    return GQA_ERR_SHAPE;
   if (o_dtype != GQA_OUT_F32 && o_dtype != GQA_OUT_BF16) return GQA_ERR_SHAPE;
   if (!scale_ok(scale)) return GQA_ERR_SHAPE;
-  if (static_cast<long long>(B) * L * h_q * d >= kMaxElems) return GQA_ERR_SHAPE;
+  if (window < 0 || (window > 0 && !causal)) return GQA_ERR_SHAPE;
+  if (static_cast<long long>(B) * Lq * h_q * d >= kMaxElems) return GQA_ERR_SHAPE;
+  if (static_cast<long long>(B) * g * kv_extent * d >= kMaxElems) return GQA_ERR_SHAPE;
   {
     // work units (pairs of 128-row query tiles x K/V heads x batch) index an int
     const long long pm2 = 2LL * (gqa::kPrefillBM / (h_q / g));
-    if ((L + pm2 - 1) / pm2 * g * B >= (1LL << 31)) return GQA_ERR_SHAPE;
+    if ((Lq + pm2 - 1) / pm2 * g * B >= (1LL << 31)) return GQA_ERR_SHAPE;
   }
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o)) return GQA_ERR_ALIGN;
   if (lse != nullptr && !aligned4(lse)) return GQA_ERR_ALIGN;
+  if (alibi != nullptr && !aligned4(alibi)) return GQA_ERR_ALIGN;
+  if (kv_lens != nullptr && !aligned4(kv_lens)) return GQA_ERR_ALIGN;
   if (status_dev != nullptr && !aligned4(status_dev)) return GQA_ERR_ALIGN;
 
   const int G = h_q / g;
@@ -143,16 +157,16 @@ int gqa_prefill_fwd(const void* q, const void* k, const void* v, void* o, int o_
   const cuuint64_t e = 2;  // bytes per bf16
   {
     const cuuint64_t dims[4] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(h_q),
-                                static_cast<cuuint64_t>(L), static_cast<cuuint64_t>(B)};
+                                static_cast<cuuint64_t>(Lq), static_cast<cuuint64_t>(B)};
     const cuuint64_t strides[3] = {d * e, static_cast<cuuint64_t>(h_q) * d * e,
-                                   static_cast<cuuint64_t>(L) * h_q * d * e};
+                                   static_cast<cuuint64_t>(Lq) * h_q * d * e};
     const cuuint32_t box[4] = {64, static_cast<cuuint32_t>(G),
                                static_cast<cuuint32_t>(gqa::kPrefillBM / G), 1};
     if (!encode_bf16(&a.tm_q, 4, q, dims, strides, box)) return GQA_ERR_CUDA;
     // the output has the query layout; boxes are 128-byte column chunks
     const cuuint64_t oe = o_dtype == GQA_OUT_F32 ? 4 : 2;
     const cuuint64_t ostrides[3] = {d * oe, static_cast<cuuint64_t>(h_q) * d * oe,
-                                    static_cast<cuuint64_t>(L) * h_q * d * oe};
+                                    static_cast<cuuint64_t>(Lq) * h_q * d * oe};
     const cuuint32_t obox[4] = {static_cast<cuuint32_t>(128 / oe), static_cast<cuuint32_t>(G),
                                 static_cast<cuuint32_t>(gqa::kPrefillBM / G), 1};
     if (!encode_sw128(&a.tm_o, o_dtype == GQA_OUT_F32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32
@@ -160,20 +174,30 @@ int gqa_prefill_fwd(const void* q, const void* k, const void* v, void* o, int o_
                       4, o, dims, ostrides, obox))
       return GQA_ERR_CUDA;
   }
-  {
+  if (kv_lens == nullptr) {
+    // [B, Lk, g, d]: 4-D map {d, g, Lk, B}, a box is 128 keys of one head
     const cuuint64_t dims[4] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(g),
-                                static_cast<cuuint64_t>(L), static_cast<cuuint64_t>(B)};
+                                static_cast<cuuint64_t>(kv_extent), static_cast<cuuint64_t>(B)};
     const cuuint64_t strides[3] = {d * e, static_cast<cuuint64_t>(g) * d * e,
-                                   static_cast<cuuint64_t>(L) * g * d * e};
+                                   static_cast<cuuint64_t>(kv_extent) * g * d * e};
     const cuuint32_t box[4] = {64, 1, static_cast<cuuint32_t>(gqa::kPrefillBN), 1};
     if (!encode_bf16(&a.tm_k, 4, k, dims, strides, box)) return GQA_ERR_CUDA;
     if (!encode_bf16(&a.tm_v, 4, v, dims, strides, box)) return GQA_ERR_CUDA;
+  } else {
+    // cache [B, g, S_max, d]: 3-D map {d, S_max, B*g} (as in decode)
+    const cuuint64_t dims[3] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(kv_extent),
+                                static_cast<cuuint64_t>(B) * g};
+    const cuuint64_t strides[2] = {d * e, static_cast<cuuint64_t>(kv_extent) * d * e};
+    const cuuint32_t box[3] = {64, static_cast<cuuint32_t>(gqa::kPrefillBN), 1};
+    if (!encode_bf16(&a.tm_k, 3, k, dims, strides, box)) return GQA_ERR_CUDA;
+    if (!encode_bf16(&a.tm_v, 3, v, dims, strides, box)) return GQA_ERR_CUDA;
   }
-  a.o = o;
   a.o_dtype = o_dtype;
   a.lse = lse;
   a.B = B;
-  a.L = L;
+  a.Lq = Lq;
+  a.Lk = kv_lens == nullptr ? kv_extent : 0;
+  a.S_max = kv_extent;
   a.h_q = h_q;
   a.g = g;
   a.d = d;
@@ -181,9 +205,41 @@ int gqa_prefill_fwd(const void* q, const void* k, const void* v, void* o, int o_
   a.G_log2 = log2i(G);
   a.scale_log2 = scale * 1.4426950408889634f;
   a.causal = causal != 0;
+  a.kv_lens = kv_lens;
+  a.window = window;
+  a.alibi = alibi;
   a.status = status_dev;
   return gqa::launch_prefill(a, static_cast<cudaStream_t>(stream)) == cudaSuccess ? GQA_OK
                                                                                     : GQA_ERR_CUDA;
+}
+
+}  // namespace
+
+extern "C" {
+
+int gqa_prefill_fwd(const void* q, const void* k, const void* v, void* o, int o_dtype,
+                    float* lse, int B, int L, int h_q, int g, int d, float scale, int causal,
+                    int32_t* status_dev, void* stream) {
+  return prefill_common(q, k, v, nullptr, o, o_dtype, lse, B, L, L, h_q, g, d, scale, causal, 0,
+                        nullptr, status_dev, stream);
+}
+
+int gqa_prefill_fwd_ex(const void* q, const void* k, const void* v, void* o, int o_dtype,
+                       float* lse, int B, int L, int h_q, int g, int d, float scale, int causal,
+                       int window, const float* alibi_slopes, int32_t* status_dev,
+                       void* stream) {
+  return prefill_common(q, k, v, nullptr, o, o_dtype, lse, B, L, L, h_q, g, d, scale, causal,
+                        window, alibi_slopes, status_dev, stream);
+}
+
+int gqa_prefill_kvcache_fwd(const void* q, const void* k_cache, const void* v_cache,
+                            const int32_t* seq_lens, void* o, int o_dtype, float* lse, int B,
+                            int T, int h_q, int g, int d, int S_max, float scale, int window,
+                            const float* alibi_slopes, int32_t* status_dev, void* stream) {
+  if (seq_lens == nullptr) return GQA_ERR_NULL;
+  if (T > S_max) return GQA_ERR_SHAPE;
+  return prefill_common(q, k_cache, v_cache, seq_lens, o, o_dtype, lse, B, T, S_max, h_q, g, d,
+                        scale, 1, window, alibi_slopes, status_dev, stream);
 }
 
 size_t gqa_decode_workspace_bytes(int B, int h_q, int g, int d, int S_max) {
@@ -195,12 +251,22 @@ int gqa_decode_fwd(const void* q, const void* k_cache, const void* v_cache,
                    const int32_t* seq_lens, void* o, int o_dtype, float* lse, int B, int h_q,
                    int g, int d, int S_max, float scale, void* workspace, size_t workspace_bytes,
                    int32_t* status_dev, void* stream) {
+  return gqa_decode_fwd_ex(q, k_cache, v_cache, seq_lens, o, o_dtype, lse, B, h_q, g, d, S_max,
+                           scale, 0, nullptr, workspace, workspace_bytes, status_dev, stream);
+}
+
+int gqa_decode_fwd_ex(const void* q, const void* k_cache, const void* v_cache,
+                      const int32_t* seq_lens, void* o, int o_dtype, float* lse, int B, int h_q,
+                      int g, int d, int S_max, float scale, int window,
+                      const float* alibi_slopes, void* workspace, size_t workspace_bytes,
+                      int32_t* status_dev, void* stream) {
   if (q == nullptr || k_cache == nullptr || v_cache == nullptr || seq_lens == nullptr ||
       o == nullptr)
     return GQA_ERR_NULL;
   if (!decode_shape_ok(B, h_q, g, d, S_max)) return GQA_ERR_SHAPE;
   if (o_dtype != GQA_OUT_F32 && o_dtype != GQA_OUT_BF16) return GQA_ERR_SHAPE;
-  if (!scale_ok(scale)) return GQA_ERR_SHAPE;
+  if (!scale_ok(scale) || window < 0) return GQA_ERR_SHAPE;
+  if (alibi_slopes != nullptr && !aligned4(alibi_slopes)) return GQA_ERR_ALIGN;
   const DecodeLayout lay = decode_layout(B, h_q, g, d, S_max);
   if (workspace == nullptr || workspace_bytes < lay.total) return GQA_ERR_WORKSPACE;
   if (!aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(o) ||
@@ -234,6 +300,8 @@ int gqa_decode_fwd(const void* q, const void* k_cache, const void* v_cache,
   a.split_len = lay.split_len;
   a.n_split = lay.n_split;
   a.scale_log2 = scale * 1.4426950408889634f;
+  a.window = window;
+  a.alibi = alibi_slopes;
   a.status = status_dev;
   return gqa::launch_decode(a, static_cast<cudaStream_t>(stream)) == cudaSuccess ? GQA_OK
                                                                                    : GQA_ERR_CUDA;

@@ -73,6 +73,7 @@ __device__ __forceinline__ uint32_t sw128(int row, int chunk) {
 // One decoded work item.
 struct Item {
   int b, kvh, hs, split;
+  int len;           // valid rows of the sequence (the query sits at len - 1)
   int s0, s1, n_st;  // token range [s0, s1) and its 64-token stages (0: nothing to do)
 };
 
@@ -81,7 +82,7 @@ struct Item {
 // partial and empty splits at the end of short sequences come last and fill
 // the tail of the pass.
 __device__ __forceinline__ Item decode_item(int u, const int32_t* seq_lens, int g, int n_hslice,
-                                            int S_max, int split_len, int n_segs) {
+                                            int S_max, int split_len, int n_segs, int window) {
   Item it;
   it.split = u / n_segs;
   const int seg = u % n_segs;
@@ -91,9 +92,12 @@ __device__ __forceinline__ Item decode_item(int u, const int32_t* seq_lens, int 
   it.b = pair / g;
   int len = seq_lens[it.b];
   len = len < 0 ? 0 : (len > S_max ? S_max : len);
-  it.s0 = it.split * split_len;
-  it.s1 = min(len, it.s0 + split_len);
-  it.n_st = it.s0 < len ? (it.s1 - it.s0 + kDecodeStage - 1) / kDecodeStage : 0;
+  it.len = len;
+  // rows before the sliding window (if any) are not read at all
+  const int lo = window > 0 ? max(0, len - window) : 0;
+  it.s0 = max(it.split * split_len, lo);
+  it.s1 = min(len, it.split * split_len + split_len);
+  it.n_st = it.s0 < it.s1 ? (it.s1 - it.s0 + kDecodeStage - 1) / kDecodeStage : 0;
   return it;
 }
 
@@ -106,7 +110,8 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) decode_split_kernel(
     const __nv_bfloat16* __restrict__ q, const int32_t* __restrict__ seq_lens,
     float* __restrict__ part_o, float* __restrict__ part_lse, int h_q, int g, int G,
     int n_hslice, int S_max, int split_len, int n_split, int n_items, float scale_log2,
-    int* __restrict__ item_counter, int32_t* status) {
+    int window, const float* __restrict__ alibi, int* __restrict__ item_counter,
+    int32_t* status) {
   using C = DecCfg<D>;
   constexpr int kStages = C::kStages;
   constexpr int kCB = C::kCB;
@@ -147,7 +152,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) decode_split_kernel(
       // so CTAs that drew short items simply fetch more
       for (int u = atomicAdd(item_counter, 1); u < n_items && ok;
            u = atomicAdd(item_counter, 1)) {
-        const Item it = decode_item(u, seq_lens, g, n_hslice, S_max, split_len, n_segs);
+        const Item it = decode_item(u, seq_lens, g, n_hslice, S_max, split_len, n_segs, window);
         const int zrow = it.b * g + it.kvh;
         for (int st = 0; st < it.n_st; ++st, ++sc) {
           const int slot = sc % kStages;
@@ -201,6 +206,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) decode_split_kernel(
     float o_acc[D / 8][4];
     float m_r[2] = {-INFINITY, -INFINITY};  // running max (log2 units), stale by < 2^8
     float l_r[2] = {0.f, 0.f};
+    float slope[2] = {0.f, 0.f};
     while (ok) {
       const int slot = sc % kStages;
       ok = __all_sync(0xffffffffu, mbar_wait(&full_bar[slot], (sc / kStages) & 1, &abort_flag));
@@ -210,7 +216,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) decode_split_kernel(
       const int st = tg.y;
       if (st == 0) {
         // a new item: its query rows and fresh accumulators
-        it = decode_item(tg.x, seq_lens, g, n_hslice, S_max, split_len, n_segs);
+        it = decode_item(tg.x, seq_lens, g, n_hslice, S_max, split_len, n_segs, window);
         head0 = static_cast<size_t>(it.b) * h_q + static_cast<size_t>(it.kvh) * G + it.hs * 32;
         Gs = min(G - it.hs * 32, 16 * MT);  // stacked rows served by this item
         const __nv_bfloat16* qg = q + head0 * D;
@@ -226,6 +232,15 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) decode_split_kernel(
         for (int i = 0; i < D / 8; ++i) o_acc[i][0] = o_acc[i][1] = o_acc[i][2] = o_acc[i][3] = 0.f;
         m_r[0] = m_r[1] = -INFINITY;
         l_r[0] = l_r[1] = 0.f;
+        if (alibi != nullptr) {
+          // ALiBi slopes of this lane's two rows, in log2 units of the scaled score
+          slope[0] = row0 < Gs ? alibi[head0 - static_cast<size_t>(it.b) * h_q + row0] *
+                                     1.4426950408889634f
+                               : 0.f;
+          slope[1] = row1 < Gs ? alibi[head0 - static_cast<size_t>(it.b) * h_q + row1] *
+                                     1.4426950408889634f
+                               : 0.f;
+        }
       }
       const int tok0 = it.s0 + st * kDecodeStage;
       const int valid = it.s1 - tok0;  // rows of this stage that are real
@@ -290,7 +305,11 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) decode_split_kernel(
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
               const int tok = r0[sb] + j * 8 + tq * 2 + (e & 1);
-              const float x = act[sb] && tok < valid ? s[sb][j][e] * scale_log2 : -INFINITY;
+              // ALiBi: -slope * (query position - key position)
+              const float bias =
+                  slope[e >> 1] * static_cast<float>(tok0 + tok - (it.len - 1));
+              const float x =
+                  act[sb] && tok < valid ? fmaf(s[sb][j][e], scale_log2, bias) : -INFINITY;
               s[sb][j][e] = x;
               mx[e >> 1] = fmaxf(mx[e >> 1], x);
             }
@@ -322,6 +341,8 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) decode_split_kernel(
         // all-masked so far: keep everything at zero weight
         const float m_use[2] = {m_r[0] == -INFINITY ? 0.f : m_r[0],
                                 m_r[1] == -INFINITY ? 0.f : m_r[1]};
+        // P in bf16 (the A operand of P.V); the row sums add the same rounded
+        // weights, so numerator and denominator round alike
         float rs[2] = {0.f, 0.f};
 #pragma unroll
         for (int sb = 0; sb < kSubPerWarp; ++sb)
@@ -329,7 +350,8 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) decode_split_kernel(
           for (int j = 0; j < 2; ++j)
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
-              const float p = ex2_approx(s[sb][j][e] - m_use[e >> 1]);
+              const float p = __bfloat162float(__float2bfloat16_rn(
+                  ex2_approx(s[sb][j][e] - m_use[e >> 1])));
               s[sb][j][e] = p;
               rs[e >> 1] += p;
             }
@@ -407,7 +429,7 @@ __global__ void __launch_bounds__(kCombineThreads) decode_combine_kernel(
     const float* __restrict__ part_o, const float* __restrict__ part_lse,
     const int32_t* __restrict__ seq_lens, void* __restrict__ o, int o_dtype,
     float* __restrict__ lse_out, int h_q, int S_max, int split_len, int n_split, int n_slices,
-    int32_t* status) {
+    int window, int32_t* status) {
   constexpr int kLanesPerRow = D / 4;                       // threads covering one row
   constexpr int kGroups = kCombineThreads / kLanesPerRow;   // partial groups
   constexpr int kWarps = kCombineThreads / 32;
@@ -424,9 +446,11 @@ __global__ void __launch_bounds__(kCombineThreads) decode_combine_kernel(
   }
   // partials of this row: n_slices per split (one per token slice; a slice
   // that saw no token holds lse = -inf and weighs nothing)
-  const int n = (len + split_len - 1) / split_len * n_slices;
+  // splits wholly before the sliding window were never written
+  const int first = (window > 0 ? max(0, len - window) : 0) / split_len * n_slices;
+  const int n = (len + split_len - 1) / split_len * n_slices - first;
   const int n_part = n_split * n_slices;
-  const float* pl = part_lse + static_cast<size_t>(bh) * n_part;
+  const float* pl = part_lse + static_cast<size_t>(bh) * n_part + first;
   const bool staged = n <= kCombineSmem;
   auto lse_at = [&](int s) { return staged ? wsh[s] : pl[s]; };
   // block max of the partial log-sum-exps
@@ -461,7 +485,7 @@ __global__ void __launch_bounds__(kCombineThreads) decode_combine_kernel(
   // weighted sum of the partial outputs
   const int grp = tid / kLanesPerRow;
   const int c4 = (tid % kLanesPerRow) * 4;
-  const float* po = part_o + static_cast<size_t>(bh) * n_part * D + c4;
+  const float* po = part_o + (static_cast<size_t>(bh) * n_part + first) * D + c4;
   float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll 4
   for (int s = grp; s < n; s += kGroups) {
@@ -556,13 +580,13 @@ static cudaError_t launch_decode_t(const DecodeArgs& a, cudaStream_t s) {
   decode_split_kernel<D, MT><<<grid, kThreads, kSmem, s>>>(
       a.tm_k, a.tm_v, static_cast<const __nv_bfloat16*>(a.q), a.seq_lens, a.part_o, a.part_lse,
       a.h_q, a.g, a.G, n_hslice, a.S_max, a.split_len, a.n_split, static_cast<int>(n_items),
-      a.scale_log2, a.item_counter, a.status);
+      a.scale_log2, a.window, a.alibi, a.item_counter, a.status);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   decode_combine_kernel<D><<<a.B * a.h_q, kCombineThreads, 0, s>>>(a.part_o, a.part_lse, a.seq_lens, a.o,
                                                       a.o_dtype, a.lse, a.h_q, a.S_max,
                                                       a.split_len, a.n_split, kConsumers / MT,
-                                                      a.status);
+                                                      a.window, a.status);
   return cudaGetLastError();
 }
 

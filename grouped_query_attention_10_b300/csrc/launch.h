@@ -20,14 +20,16 @@ constexpr int kDecodeStage = 64;
 constexpr int kDecodeSlices = 4;
 
 struct PrefillArgs {
-  CUtensorMap tm_q, tm_k, tm_v;
+  CUtensorMap tm_q, tm_k, tm_v;  // K/V maps are {d, g, keys, B} in either K/V layout
   CUtensorMap tm_o;  // output, 128-byte-wide column chunks (32 fp32 or 64 bf16)
-  void* o;
   int o_dtype;
   float* lse;
-  int B, L, h_q, g, d, G, G_log2;
+  int B, Lq, Lk, S_max, h_q, g, d, G, G_log2;
   float scale_log2;  // softmax scale * log2(e)
   int causal;
+  const int32_t* kv_lens;  // per-sequence key counts (K/V from a cache), or nullptr
+  int window;              // sliding window (causal only), 0: none
+  const float* alibi;      // per-query-head ALiBi slopes, or nullptr
   int32_t* status;
 };
 
@@ -43,6 +45,8 @@ struct DecodeArgs {
   int* item_counter; // work-item counter of the split pass (zeroed before each launch)
   int B, h_q, g, d, G, S_max, split_len, n_split;
   float scale_log2;
+  int window;          // sliding window (the last `window` rows), 0: none
+  const float* alibi;  // per-query-head ALiBi slopes, or nullptr
   int32_t* status;
 };
 

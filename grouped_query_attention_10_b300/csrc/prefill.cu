@@ -100,14 +100,31 @@ struct PrefillCfg {
   static constexpr uint32_t kStrideP = kSepP ? BN / 2 : BN;   // P_t at kColP + t * kStrideP
 };
 
+// Runtime sizes and options of one launch (kernel parameter, read-only).
+struct PrefillParams {
+  float* lse;                // [B, h_q, Lq] natural-log sum-exp, or nullptr
+  int o_dtype;
+  int B, Lq, Lk, S_max;      // Lk: keys per sequence unless kv_lens is given
+  int h_q, g, G, G_log2;
+  float scale_log2;          // softmax scale * log2(e)
+  int n_ctiles, n_units;
+  const int32_t* kv_lens;    // per-sequence key counts (K/V read from a cache), or nullptr
+  int window;                // sliding window in keys (causal only), 0: none
+  const float* alibi;        // per-query-head ALiBi slopes (natural units), or nullptr
+  int32_t* status;
+};
+
 // One decoded work unit.
 struct Unit {
   int b, kvh, p0;  // batch, K/V head, first position of query tile 0
-  int n0, n1;      // K/V tiles seen by query tile 0 / 1 (n1 = 0: tile 1 lies past L)
+  int Lk, q_off;   // keys of this sequence; query position i sits at key position i + q_off
+  int kv0;         // first K/V tile the unit reads (all earlier keys are outside the window)
+  int n0, n1;      // K/V tiles from kv0 on seen by query tile 0 / 1 (n1 = 0: tile 1 past Lq)
 };
 
-__device__ __forceinline__ Unit decode_unit(int u, int n_ctiles, int g, int L, int PM,
-                                            bool causal, int n_pairs, int n_units) {
+__device__ __forceinline__ Unit decode_unit(int u, const PrefillParams& p, int PM, bool causal,
+                                            bool windowed, bool cached) {
+  const int n_pairs = p.g * p.B;  // (batch, K/V head) pairs
   int ct, pair;
   if (causal) {
     // longest units first (later query tiles see more keys), dealt to the
@@ -115,23 +132,39 @@ __device__ __forceinline__ Unit decode_unit(int u, int n_ctiles, int g, int L, i
     // total work comes out nearly equal
     const int G0 = static_cast<int>(gridDim.x);
     const int round = u / G0;
-    const bool flip = (round & 1) && (round + 1) * G0 <= n_units;  // full rounds only
+    const bool flip = (round & 1) && (round + 1) * G0 <= p.n_units;  // full rounds only
     const int r = flip ? round * G0 + (G0 - 1 - u % G0) : u;
-    ct = n_ctiles - 1 - r / n_pairs;
+    ct = p.n_ctiles - 1 - r / n_pairs;
     pair = r % n_pairs;
   } else {
     // consecutive units share the (batch, K/V head), so CTAs that run at the
     // same time read the same K/V tiles and hit in L2
-    ct = u % n_ctiles;
-    pair = u / n_ctiles;
+    ct = u % p.n_ctiles;
+    pair = u / p.n_ctiles;
   }
   Unit w;
-  w.kvh = pair % g;
-  w.b = pair / g;
+  w.kvh = pair % p.g;
+  w.b = pair / p.g;
   w.p0 = ct * 2 * PM;
-  const int all = (L + BN - 1) / BN;
-  w.n0 = causal ? (min(L, w.p0 + PM) + BN - 1) / BN : all;
-  w.n1 = w.p0 + PM < L ? (causal ? (min(L, w.p0 + 2 * PM) + BN - 1) / BN : all) : 0;
+  w.Lk = p.Lk;
+  if (cached) {
+    // keys in the cache; the new queries are its last Lq rows
+    const int n = p.kv_lens[w.b];
+    w.Lk = n < p.Lq ? p.Lq : (n > p.S_max ? p.S_max : n);
+  }
+  w.q_off = causal ? w.Lk - p.Lq : 0;
+  const int lo0 = windowed ? max(0, w.q_off + w.p0 - p.window + 1) : 0;
+  w.kv0 = lo0 / BN;
+  const int last0 = min(p.Lq, w.p0 + PM) - 1;
+  const int hi0 = causal ? min(w.Lk - 1, w.q_off + last0) : w.Lk - 1;
+  w.n0 = hi0 / BN - w.kv0 + 1;
+  if (w.p0 + PM < p.Lq) {
+    const int last1 = min(p.Lq, w.p0 + 2 * PM) - 1;
+    const int hi1 = causal ? min(w.Lk - 1, w.q_off + last1) : w.Lk - 1;
+    w.n1 = hi1 / BN - w.kv0 + 1;
+  } else {
+    w.n1 = 0;
+  }
   return w;
 }
 
@@ -146,12 +179,17 @@ __device__ __forceinline__ void drain_ring(uint64_t* full, int depth, int issued
 
 }  // namespace
 
-template <int D, bool CAUSAL>
+// VAR: bit 0 = sliding window, bit 1 = ALiBi bias, bit 2 = K/V read from a
+// [B, g, S_max, d] cache with per-sequence key counts (chunked prefill).
+template <int D, bool CAUSAL, int VAR>
 __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(
     const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
     const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_o,
-    int o_dtype, float* __restrict__ lse, int B, int L, int h_q, int g, int G, int G_log2, float scale_log2,
-    int n_ctiles, int n_units, int32_t* status) {
+    const PrefillParams p) {
+  constexpr bool kWindow = (VAR & 1) != 0;
+  constexpr bool kAlibi = (VAR & 2) != 0;
+  constexpr bool kCache = (VAR & 4) != 0;
+  const int g = p.g, G = p.G, G_log2 = p.G_log2, h_q = p.h_q, n_units = p.n_units;
   using C = PrefillCfg<D>;
   constexpr int KS = C::KS;
   constexpr int VS = C::VS;
@@ -184,7 +222,6 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const int PM = BM >> G_log2;  // positions per query tile
-  const int n_pairs = g * B;    // (batch, K/V head) pairs
 
   if (threadIdx.x == 0) {
     abort_flag = 0;
@@ -235,7 +272,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(
       int nu = 0, kc = 0, vc = 0;  // units, K tiles and V tiles issued so far
       bool ok = true;
       for (int u = blockIdx.x; u < n_units && ok; u += gridDim.x, ++nu) {
-        const Unit w = decode_unit(u, n_ctiles, g, L, PM, CAUSAL, n_pairs, n_units);
+        const Unit w = decode_unit(u, p, PM, CAUSAL, kWindow, kCache);
         const int n_kv = max(w.n0, w.n1);
         const int qs = nu % NQ;
         if (nu >= NQ) ok = mbar_wait(&bar_qe[qs], ((nu / NQ) - 1) & 1, &abort_flag);
@@ -254,18 +291,26 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(
           if (!ok) break;
           mbar_arrive_expect_tx(&bar_kf[ks], C::kKVStage);
 #pragma unroll
-          for (int cb = 0; cb < D / 64; ++cb)
-            tma_load_4d(smem + C::kOffK + ks * C::kKVStage + cb * (BN * 128), &tm_k,
-                        &bar_kf[ks], cb * 64, w.kvh, j * BN, w.b);
+          for (int cb = 0; cb < D / 64; ++cb) {
+            uint8_t* dst = smem + C::kOffK + ks * C::kKVStage + cb * (BN * 128);
+            if (kCache)  // 3-D map over the cache
+              tma_load_3d(dst, &tm_k, &bar_kf[ks], cb * 64, (w.kv0 + j) * BN, w.b * g + w.kvh);
+            else
+              tma_load_4d(dst, &tm_k, &bar_kf[ks], cb * 64, w.kvh, (w.kv0 + j) * BN, w.b);
+          }
           ++kc;
           const int vs = vc % VS;
           if (vc >= VS) ok = mbar_wait(&bar_ve[vs], ((vc / VS) - 1) & 1, &abort_flag);
           if (!ok) break;
           mbar_arrive_expect_tx(&bar_vf[vs], C::kKVStage);
 #pragma unroll
-          for (int cb = 0; cb < D / 64; ++cb)
-            tma_load_4d(smem + C::kOffV + vs * C::kKVStage + cb * (BN * 128), &tm_v,
-                        &bar_vf[vs], cb * 64, w.kvh, j * BN, w.b);
+          for (int cb = 0; cb < D / 64; ++cb) {
+            uint8_t* dst = smem + C::kOffV + vs * C::kKVStage + cb * (BN * 128);
+            if (kCache)  // 3-D map over the cache
+              tma_load_3d(dst, &tm_v, &bar_vf[vs], cb * 64, (w.kv0 + j) * BN, w.b * g + w.kvh);
+            else
+              tma_load_4d(dst, &tm_v, &bar_vf[vs], cb * 64, w.kvh, (w.kv0 + j) * BN, w.b);
+          }
           ++vc;
         }
         if (!ok) {
@@ -339,7 +384,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(
     int it = 0;          // (unit, K/V tile) steps of this query tile so far
     bool ok = true;
     for (int u = blockIdx.x; u < n_units && ok; u += gridDim.x, ++nu) {
-      const Unit w = decode_unit(u, n_ctiles, g, L, PM, CAUSAL, n_pairs, n_units);
+      const Unit w = decode_unit(u, p, PM, CAUSAL, kWindow, kCache);
       const int n_kv = max(w.n0, w.n1);
       const int n_me = t == 0 ? w.n0 : w.n1;
       const int qs = nu % NQ;
@@ -354,13 +399,25 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(
         if (leader) issue_s(qs, kb % KS);
         __syncwarp();
       }
-      // the query slot is free once this tile's last score product retires
+      // the query slot is free once this tile's last score product retires;
+      // a tile without keys gives it back only once it has landed (a plain
+      // arrive must never run ahead of the fill it releases)
+      if (n_me == 0) {
+        ok = wait_all(&bar_q[qs], (nu / NQ) & 1);
+        if (!ok) break;
+      }
       if (n_me <= 1) release(&bar_qe[qs], n_me == 1);
       for (int j = 0; ok && j < n_kv; ++j) {
         const int kj = kb + j;  // ring index of K/V tile j
         if (j >= n_me) {
-          // this query tile sees no keys from tile j on
+          // this query tile sees no keys from tile j on: give the slots back,
+          // each only after its fill has landed, so this issuer can never
+          // arrive twice on a slot before the other issuer has used it
+          ok = wait_all(&bar_kf[kj % KS], (kj / KS) & 1);
+          if (!ok) break;
           release(&bar_ke[kj % KS], false);
+          ok = wait_all(&bar_vf[kj % VS], (kj / VS) & 1);
+          if (!ok) break;
           release(&bar_ve[kj % VS], false);
           continue;
         }
@@ -423,23 +480,38 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(
     const uint32_t t_s = tmem + lane_base + static_cast<uint32_t>(t) * BN;
     const uint32_t t_o = tmem + lane_base + C::kColO + static_cast<uint32_t>(t) * D;
     const uint32_t t_p = tmem + lane_base + C::kColP + static_cast<uint32_t>(t) * C::kStrideP;
+    const float scale_log2 = p.scale_log2;
     const uint64_t c2 = f32x2(scale_log2, scale_log2);
-    int it = 0;     // (unit, K/V tile) steps of this query tile so far
-    int npass = 0;  // output staging passes of this query tile so far
-    int kturn = 0;  // exponential phases of both tiles in earlier units
+    int it = 0;      // (unit, K/V tile) steps of this query tile so far
+    int npass = 0;   // output staging passes of this query tile so far
+    int kturn = 0;   // exponential phases of both tiles in earlier units
+    int kvbase = 0;  // K/V tiles of earlier units (ring index of this unit's first tile)
     bool ok = true;
     for (int u = blockIdx.x; u < n_units && ok; u += gridDim.x) {
-      const Unit w = decode_unit(u, n_ctiles, g, L, PM, CAUSAL, n_pairs, n_units);
+      const Unit w = decode_unit(u, p, PM, CAUSAL, kWindow, kCache);
       const int n_my = t == 0 ? w.n0 : w.n1;
+      const int n_kv = max(w.n0, w.n1);
+      if (kCache && threadIdx.x == 128 && w.kvh == 0 && w.p0 == 0) {
+        const int n = p.kv_lens[w.b];
+        if (n < p.Lq || n > p.S_max) record_status(p.status, GQA_ERR_BAD_LENGTH);
+      }
       if (n_my == 0) {
         kturn += w.n0 + w.n1;  // this tile sees no keys in this unit
+        kvbase += n_kv;
         continue;
       }
       const int pt = w.p0 + t * PM;
       const int pos = pt + (row >> G_log2);
       const int head = w.kvh * G + (row & (G - 1));
-      const int last_key = CAUSAL ? min(L - 1, pos) : L - 1;  // last key this row may see
-      float m_run = -INFINITY;  // running max of scale*log2(e)*s, possibly stale by < 2^8
+      const int q_abs = w.q_off + pos;  // key position of this row's query
+      // keys this row may see: [first_key, last_key]
+      const int last_key = CAUSAL ? min(w.Lk - 1, q_abs) : w.Lk - 1;
+      const int first_key = kWindow ? q_abs - p.window + 1 : 0;
+      // last query row of the tile, for the tile-level mask decisions
+      const int q_abs_last = w.q_off + min(p.Lq, pt + PM) - 1;
+      // ALiBi: -slope * |q_abs - key| in log2 units of the scaled score
+      const float slope_log2 = kAlibi ? p.alibi[head] * 1.4426950408889634f : 0.f;
+      float m_run = -INFINITY;  // running max of the log2-unit scores, possibly stale by < 2^8
       float l_run = 0.f;
       for (int j = 0; j < n_my; ++j) {
         ok = __all_sync(0xffffffffu, mbar_wait(&bar_s[t], (it + j) & 1, &abort_flag));
@@ -454,13 +526,24 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(
           tc_fence_before();
           mbar_arrive(&bar_sf[t]);
         }
-        const int key0 = j * BN;
-        const bool need_mask = (key0 + BN > L) || (CAUSAL && key0 + BN - 1 > pt);
-        if (need_mask) {
-          const int nvis = last_key - key0;  // tile columns e <= nvis are visible
+        const int key0 = (w.kv0 + j) * BN;
+        const bool need_mask = (key0 + BN > w.Lk) || (CAUSAL && key0 + BN - 1 > w.q_off + pt) ||
+                               (kWindow && key0 <= q_abs_last - p.window);
+        if (kAlibi) {
+          // biased log2-unit scores; masked keys become -inf
 #pragma unroll
-          for (int e = 0; e < BN; ++e)
-            if (e > nvis) r[e] = 0xff800000u;  // -inf
+          for (int e = 0; e < BN; ++e) {
+            const int key = key0 + e;
+            const float bias = -slope_log2 * static_cast<float>(abs(q_abs - key));
+            const float x = fmaf(__uint_as_float(r[e]), scale_log2, bias);
+            r[e] = __float_as_uint(key > last_key || key < first_key ? -INFINITY : x);
+          }
+        } else if (need_mask) {
+#pragma unroll
+          for (int e = 0; e < BN; ++e) {
+            const int key = key0 + e;
+            if (key > last_key || (kWindow && key < first_key)) r[e] = 0xff800000u;  // -inf
+          }
         }
         // row max (three-input max, four independent chains)
         float mx4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
@@ -468,7 +551,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(
         for (int e = 0; e < BN / 2; ++e)
           mx4[e & 3] = max3f(mx4[e & 3], __uint_as_float(r[2 * e]), __uint_as_float(r[2 * e + 1]));
         const float mx = max3f(mx4[0], mx4[1], fmaxf(mx4[2], mx4[3]));
-        const float m_new = fmaxf(m_run, mx * scale_log2);
+        const float m_new = fmaxf(m_run, kAlibi ? mx : mx * scale_log2);
         const bool rescale = __any_sync(0xffffffffu, m_new > m_run + kRescaleThreshold);
         float alpha = 1.f;
         if (rescale) {
@@ -511,7 +594,10 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(
         }
         // P = 2^(s * scale * log2(e) - m_run) as bf16 pairs, 64 keys at a time;
         // scale-and-shift and the running sum use packed two-lane fp32 ops
-        const uint64_t nm2 = f32x2(-m_run, -m_run);
+        // a row that has seen no key yet keeps m_run = -inf: shift by 0 instead
+        const float m_use = m_run == -INFINITY ? 0.f : m_run;
+        const uint64_t nm2 = f32x2(-m_use, -m_use);
+        const uint64_t one2 = f32x2(1.f, 1.f);
         uint64_t sum2[2] = {0ull, 0ull};
 #pragma unroll
         for (int hh = 0; hh < 2; ++hh) {
@@ -520,15 +606,40 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(
           for (int e = 0; e < 32; ++e) {
             const int c = hh * 64 + 2 * e;
             float xa, xb;
-            split_f32x2(ffma_x2(u32x2(r[c], r[c + 1]), c2, nm2), xa, xb);
+            split_f32x2(ffma_x2(u32x2(r[c], r[c + 1]), kAlibi ? one2 : c2, nm2), xa, xb);
             const float pa = ex2_approx(xa);
             const float pb = ex2_approx(xb);
-            sum2[e & 1] = fadd_x2(sum2[e & 1], f32x2(pa, pb));
             pw[e] = pack_bf16x2(pa, pb);
+            if (kAlibi) {
+              // ALiBi makes rows peaked (one weight near 1): sum the bf16
+              // weights the P.V product really uses, so numerator and
+              // denominator round alike
+              sum2[e & 1] = fadd_x2(sum2[e & 1], u32x2(pw[e] << 16, pw[e] & 0xffff0000u));
+            } else {
+              sum2[e & 1] = fadd_x2(sum2[e & 1], f32x2(pa, pb));
+            }
           }
           tmem_st32(t_p + hh * 32, pw);  // P columns [32hh, 32hh+32) = keys [64hh, 64hh+64)
         }
         mbar_arrive(&bar_turn[wq]);  // this warp's exponential phase is over
+        if (kCache && key0 + BN > w.Lk) {
+          // cache rows past the sequence may hold anything (even NaN) and
+          // 0 * NaN would poison P.V: zero them in this V stage (both query
+          // tiles may write the same zeros) once the stage has landed
+          const int vslot = (kvbase + j) % VS;
+          ok = __all_sync(0xffffffffu, mbar_wait(&bar_vf[vslot], ((kvbase + j) / VS) & 1,
+                                                  &abort_flag));
+          if (!ok) break;
+          uint8_t* vst = smem + C::kOffV + vslot * C::kKVStage;
+          const int r_lo = max(0, w.Lk - key0);
+          for (int i = threadIdx.x - 128 - 128 * t; i < (BN - r_lo) * (D / 64) * 8; i += 128) {
+            const int rr = r_lo + i / ((D / 64) * 8);
+            const int cb = (i / 8) % (D / 64);
+            *reinterpret_cast<uint4*>(vst + cb * (BN * 128) + rr * 128 + (i % 8) * 16) =
+                make_uint4(0u, 0u, 0u, 0u);
+          }
+          fence_proxy_async_smem();  // visible to the tensor core's reads of V
+        }
         tmem_st_wait();
         tc_fence_before();
         mbar_arrive(&bar_p[t]);
@@ -544,11 +655,12 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(
       tc_fence_after();
       it += n_my;
       kturn += w.n0 + w.n1;
-      const float inv_l = 1.f / l_run;
+      kvbase += n_kv;
+      const float inv_l = l_run > 0.f ? 1.f / l_run : 0.f;  // a row with no key writes zeros
       // O_t / l: staged in shared memory (128-byte swizzle, so the row-per-
       // thread writes spread over all banks) and stored by TMA in 128-byte
       // column chunks; rows past L are dropped by the store itself
-      const bool f32 = o_dtype == GQA_OUT_F32;
+      const bool f32 = p.o_dtype == GQA_OUT_F32;
       const int n_chunks = f32 ? D / 32 : D / 64;
       const bool wg_leader = threadIdx.x == 128 + 128 * t;
       uint8_t* stage = smem + C::kOffStage + t * C::kStageBytes;
@@ -613,10 +725,10 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(
         }
       }
       if (!ok) break;
-      const bool store = pos < L;
-      if (lse != nullptr && store)
-        lse[(static_cast<size_t>(w.b) * h_q + head) * L + pos] =
-            (m_run + __log2f(l_run)) * 0.69314718055994531f;
+      const bool store = pos < p.Lq;
+      if (p.lse != nullptr && store)
+        p.lse[(static_cast<size_t>(w.b) * h_q + head) * p.Lq + pos] =
+            l_run > 0.f ? (m_run + __log2f(l_run)) * 0.69314718055994531f : -INFINITY;
     }
     if (threadIdx.x == 128 + 128 * t) bulk_wait_all();  // output stores complete
   }
@@ -628,7 +740,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(
     tc_fence_after();
     tmem_dealloc(tmem, kTmCols);
   }
-  if (threadIdx.x == 0 && abort_flag) record_status(status, GQA_ERR_TIMEOUT);
+  if (threadIdx.x == 0 && abort_flag) record_status(p.status, GQA_ERR_TIMEOUT);
 }
 
 namespace {
@@ -646,35 +758,68 @@ int sm_count() {
 
 }  // namespace
 
-template <int D, bool CAUSAL>
+template <int D, bool CAUSAL, int VAR>
 static cudaError_t launch_prefill_t(const PrefillArgs& a, cudaStream_t s) {
   constexpr uint32_t kSmem = PrefillCfg<D>::kSmem;
   static bool attr_set = false;
   if (!attr_set) {
     // the register hand-over inside the kernel assumes the launch pool
     cudaFuncAttributes fa{};
-    cudaError_t e = cudaFuncGetAttributes(&fa, prefill_kernel<D, CAUSAL>);
+    cudaError_t e = cudaFuncGetAttributes(&fa, prefill_kernel<D, CAUSAL, VAR>);
     if (e != cudaSuccess) return e;
     if (fa.numRegs != kRegsLaunch) return cudaErrorInvalidKernelImage;
-    e = cudaFuncSetAttribute(prefill_kernel<D, CAUSAL>,
+    e = cudaFuncSetAttribute(prefill_kernel<D, CAUSAL, VAR>,
                              cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
     if (e != cudaSuccess) return e;
     attr_set = true;
   }
   const int PM = BM / a.G;
-  const int n_ctiles = (a.L + 2 * PM - 1) / (2 * PM);
+  const int n_ctiles = (a.Lq + 2 * PM - 1) / (2 * PM);
   const long long n_units = static_cast<long long>(n_ctiles) * a.g * a.B;
   const int grid = static_cast<int>(n_units < sm_count() ? n_units : sm_count());
-  prefill_kernel<D, CAUSAL><<<grid, kThreads, kSmem, s>>>(
-      a.tm_q, a.tm_k, a.tm_v, a.tm_o, a.o_dtype, a.lse, a.B, a.L, a.h_q, a.g, a.G, a.G_log2,
-      a.scale_log2, n_ctiles, static_cast<int>(n_units), a.status);
+  PrefillParams p{};
+  p.lse = a.lse;
+  p.o_dtype = a.o_dtype;
+  p.B = a.B;
+  p.Lq = a.Lq;
+  p.Lk = a.Lk;
+  p.S_max = a.S_max;
+  p.h_q = a.h_q;
+  p.g = a.g;
+  p.G = a.G;
+  p.G_log2 = a.G_log2;
+  p.scale_log2 = a.scale_log2;
+  p.n_ctiles = n_ctiles;
+  p.n_units = static_cast<int>(n_units);
+  p.kv_lens = a.kv_lens;
+  p.window = a.window;
+  p.alibi = a.alibi;
+  p.status = a.status;
+  prefill_kernel<D, CAUSAL, VAR><<<grid, kThreads, kSmem, s>>>(a.tm_q, a.tm_k, a.tm_v, a.tm_o,
+                                                              p);
   return cudaGetLastError();
 }
 
+template <int D>
+static cudaError_t launch_prefill_d(const PrefillArgs& a, cudaStream_t s) {
+  const int var =
+      (a.window > 0 ? 1 : 0) | (a.alibi != nullptr ? 2 : 0) | (a.kv_lens != nullptr ? 4 : 0);
+  if (!a.causal)  // a window or a cache needs causal attention (checked by the caller)
+    return var & 2 ? launch_prefill_t<D, false, 2>(a, s) : launch_prefill_t<D, false, 0>(a, s);
+  switch (var) {
+    case 1: return launch_prefill_t<D, true, 1>(a, s);
+    case 2: return launch_prefill_t<D, true, 2>(a, s);
+    case 3: return launch_prefill_t<D, true, 3>(a, s);
+    case 4: return launch_prefill_t<D, true, 4>(a, s);
+    case 5: return launch_prefill_t<D, true, 5>(a, s);
+    case 6: return launch_prefill_t<D, true, 6>(a, s);
+    case 7: return launch_prefill_t<D, true, 7>(a, s);
+    default: return launch_prefill_t<D, true, 0>(a, s);
+  }
+}
+
 cudaError_t launch_prefill(const PrefillArgs& a, cudaStream_t s) {
-  if (a.d == 64)
-    return a.causal ? launch_prefill_t<64, true>(a, s) : launch_prefill_t<64, false>(a, s);
-  return a.causal ? launch_prefill_t<128, true>(a, s) : launch_prefill_t<128, false>(a, s);
+  return a.d == 64 ? launch_prefill_d<64>(a, s) : launch_prefill_d<128>(a, s);
 }
 
 }  // namespace gqa

@@ -89,6 +89,52 @@ int gqa_prefill_fwd(const void* q, const void* k, const void* v, void* o,
                     float scale, int causal, int32_t* status_dev, void* stream);
 
 /*
+ * gqa_prefill_fwd_ex -- gqa_prefill_fwd with the score-bias variants the pages
+ * name: Mistral's sliding-window attention (the model table of the zeeklog.com
+ * page, section 2.4) and ALiBi's per-head distance penalty (the jsqmd.com
+ * survey, section 3.2).
+ *
+ *   window        0, or W > 0 (requires causal != 0): row i also hides every
+ *                 key j <= i - W, i.e. it sees the W keys i-W+1 .. i
+ *   alibi_slopes  NULL, or device fp32 [h_q]: slope_h * |i - j| (natural
+ *                 units) is subtracted from scale * q.k before the softmax
+ *
+ * Same layouts, ownership and errors as gqa_prefill_fwd; a window with
+ * causal == 0 or a negative window is GQA_ERR_SHAPE.
+ */
+int gqa_prefill_fwd_ex(const void* q, const void* k, const void* v, void* o, int o_dtype,
+                       float* lse, int B, int L, int h_q, int g, int d, float scale, int causal,
+                       int window, const float* alibi_slopes, int32_t* status_dev,
+                       void* stream);
+
+/*
+ * gqa_prefill_kvcache_fwd -- chunked prefill: T new tokens per sequence attend
+ * to everything already in the KV cache and, causally, to each other (the
+ * cache concatenation of the ijyty.com explainer, section 3.2, for more than
+ * one new token; bottom-right causal alignment).
+ *
+ *   q          [B, T, h_q, d] bf16, the T newest tokens of every sequence
+ *   k_cache,
+ *   v_cache    [B, g, S_max, d] bf16 that already hold those tokens' K/V
+ *              (kv_cache_append them first); rows at or past seq_lens[b]
+ *              are never used (they may hold anything, NaN included)
+ *   seq_lens   device int32 [B], rows per sequence, each in [T, S_max];
+ *              token t of sequence b sits at position seq_lens[b] - T + t
+ *              and sees rows 0 .. seq_lens[b] - T + t (within `window`)
+ *   o          [B, T, h_q, d] fp32 or bf16; lse optional fp32 [B, h_q, T]
+ *   window, alibi_slopes  as in gqa_prefill_fwd_ex (ALiBi distance measured
+ *              between cache positions)
+ *
+ * T > S_max is GQA_ERR_SHAPE; a seq_lens entry outside [T, S_max] is clamped
+ * into it and flagged GQA_ERR_BAD_LENGTH (that sequence's output is then
+ * not meaningful).
+ */
+int gqa_prefill_kvcache_fwd(const void* q, const void* k_cache, const void* v_cache,
+                            const int32_t* seq_lens, void* o, int o_dtype, float* lse, int B,
+                            int T, int h_q, int g, int d, int S_max, float scale, int window,
+                            const float* alibi_slopes, int32_t* status_dev, void* stream);
+
+/*
  * gqa_decode_workspace_bytes -- device scratch bytes gqa_decode_fwd needs for
  * these sizes (split-KV partial outputs and their log-sum-exp values).
  * Returns 0 for sizes gqa_decode_fwd would reject.
@@ -121,6 +167,19 @@ int gqa_decode_fwd(const void* q, const void* k_cache, const void* v_cache,
                    int B, int h_q, int g, int d, int S_max, float scale,
                    void* workspace, size_t workspace_bytes,
                    int32_t* status_dev, void* stream);
+
+/*
+ * gqa_decode_fwd_ex -- gqa_decode_fwd with a sliding window (the query, at
+ * position seq_lens[b] - 1, sees only the last `window` rows; 0 = all) and
+ * optional ALiBi slopes (device fp32 [h_q]; slope_h * (seq_lens[b] - 1 - j)
+ * is subtracted from the scaled score of row j). Same workspace as
+ * gqa_decode_fwd; a negative window is GQA_ERR_SHAPE.
+ */
+int gqa_decode_fwd_ex(const void* q, const void* k_cache, const void* v_cache,
+                      const int32_t* seq_lens, void* o, int o_dtype, float* lse, int B, int h_q,
+                      int g, int d, int S_max, float scale, int window,
+                      const float* alibi_slopes, void* workspace, size_t workspace_bytes,
+                      int32_t* status_dev, void* stream);
 
 /*
  * kv_cache_append -- write T new tokens per sequence behind its valid rows

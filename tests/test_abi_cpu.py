@@ -127,3 +127,30 @@ def test_missing_library_fails_loudly(monkeypatch, tmp_path):
     monkeypatch.setattr(binding, "LIB_PATH", str(tmp_path / "absent.so"))
     with pytest.raises(ImportError):
         binding.load_library()
+
+
+def test_variant_entry_points_validation(lib):
+    f = FAKE
+
+    def pre(causal=1, window=0, alibi=None, L=128):
+        return lib.gqa_prefill_fwd_ex(f, f, f, f, 0, None, 1, L, 8, 2, 64, 0.125, causal, window,
+                                      alibi, None, None)
+    assert pre(window=-1) == binding.GQA_ERR_SHAPE
+    assert pre(causal=0, window=16) == binding.GQA_ERR_SHAPE   # a window needs causal
+    assert pre(alibi=FAKE + 2) == binding.GQA_ERR_ALIGN
+
+    def cached(lens=f, T=16, S=1024, window=0):
+        return lib.gqa_prefill_kvcache_fwd(f, f, f, lens, f, 0, None, 2, T, 32, 8, 128, S,
+                                           0.088, window, None, None, None)
+    assert cached(lens=None) == binding.GQA_ERR_NULL
+    assert cached(T=2048, S=1024) == binding.GQA_ERR_SHAPE     # more new tokens than rows
+    assert cached(T=0) == binding.GQA_ERR_SHAPE
+    assert cached(window=-3) == binding.GQA_ERR_SHAPE
+    assert cached(lens=FAKE + 2) == binding.GQA_ERR_ALIGN
+
+    ws = lib.gqa_decode_workspace_bytes(4, 32, 8, 128, 1024)
+    def dec(window=0, alibi=None):
+        return lib.gqa_decode_fwd_ex(f, f, f, f, f, 0, None, 4, 32, 8, 128, 1024, 0.088, window,
+                                     alibi, f, ws, None, None)
+    assert dec(window=-1) == binding.GQA_ERR_SHAPE
+    assert dec(alibi=FAKE + 1) == binding.GQA_ERR_ALIGN

@@ -1,0 +1,253 @@
+"""GPU parity of the score-bias variants and the chunked prefill over a cache.
+
+Sliding window and ALiBi (the variants the pages name) on prefill and
+decode, and the chunked prefill in which T new tokens attend to a
+[B, g, S_max, d] KV cache, all through the C interface against the fp64
+oracle on the same seeded bf16 inputs. Tolerance as in the other parity
+tests: max abs error <= 1e-2, mean abs error <= 1e-3.
+"""
+
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from grouped_query_attention_10_b300 import binding as gqa
+from grouped_query_attention_10_b300 import inputs
+
+pytestmark = pytest.mark.gpu
+
+MAX_ABS = 1e-2
+MEAN_ABS = 1e-3
+DEV = "cuda"
+
+
+def f64(t):
+    return t.detach().to("cpu").to(torch.float64).numpy()
+
+
+def assert_close(got, ref, what, max_abs=MAX_ABS, mean_abs=MEAN_ABS):
+    got = np.asarray(got, dtype=np.float64)
+    ref = np.asarray(ref, dtype=np.float64)
+    assert got.shape == ref.shape, (what, got.shape, ref.shape)
+    fin = np.isfinite(ref)
+    assert np.array_equal(np.isfinite(got), fin), f"{what}: non-finite entries differ"
+    err = np.abs(got[fin] - ref[fin])
+    assert err.max() <= max_abs, f"{what}: max abs err {err.max():.3e}"
+    assert err.mean() <= mean_abs, f"{what}: mean abs err {err.mean():.3e}"
+
+
+def rand_bf16(shape, seed):
+    return inputs.random_bf16(shape, seed, device="cpu").to(DEV)
+
+
+def alibi_slopes(h_q):
+    # the usual geometric slopes 2^(-8 h / h_q), h = 1 .. h_q
+    return torch.tensor([2.0 ** (-8.0 * (h + 1) / h_q) for h in range(h_q)],
+                        dtype=torch.float32, device=DEV)
+
+
+# ---------------------------------------------------------------------------
+# prefill: sliding window and ALiBi
+# ---------------------------------------------------------------------------
+
+@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("L,window", [(200, 1), (384, 100), (300, 128), (257, 129),
+                                      (1000, 256), (129, 500)])
+def test_prefill_sliding_window(d, L, window):
+    B, h_q, g = 2, 8, 2
+    q = rand_bf16((B, L, h_q, d), 300 + L)
+    k = rand_bf16((B, L, g, d), 301 + L)
+    v = rand_bf16((B, L, g, d), 302 + L)
+    scale = 1.0 / math.sqrt(d)
+    lse = torch.empty((B, h_q, L), dtype=torch.float32, device=DEV)
+    o = gqa.gqa_prefill_fwd(q, k, v, causal=True, scale=scale, window=window, lse=lse)
+    torch.cuda.synchronize()
+    o_ref, lse_ref = oracle.prefill(f64(q), f64(k), f64(v), True, scale, window=window)
+    assert_close(f64(o), o_ref, f"window {window} L={L} d={d}")
+    assert_close(f64(lse), lse_ref, "lse")
+
+
+@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("causal", [True, False])
+@pytest.mark.parametrize("h_q,g", [(8, 2), (32, 8), (16, 16)])
+def test_prefill_alibi(d, causal, h_q, g):
+    B, L = 2, 300
+    q = rand_bf16((B, L, h_q, d), 400 + h_q + g)
+    k = rand_bf16((B, L, g, d), 401 + h_q + g)
+    v = rand_bf16((B, L, g, d), 402 + h_q + g)
+    scale = 1.0 / math.sqrt(d)
+    slopes = alibi_slopes(h_q)
+    lse = torch.empty((B, h_q, L), dtype=torch.float32, device=DEV)
+    o = gqa.gqa_prefill_fwd(q, k, v, causal=causal, scale=scale, alibi_slopes=slopes, lse=lse)
+    torch.cuda.synchronize()
+    o_ref, lse_ref = oracle.prefill(f64(q), f64(k), f64(v), causal, scale,
+                                    alibi_slopes=slopes.cpu().numpy().astype(np.float64))
+    assert_close(f64(o), o_ref, f"alibi causal={causal} h_q={h_q} g={g}")
+    assert_close(f64(lse), lse_ref, "lse", max_abs=2e-2)
+
+
+def test_prefill_window_and_alibi_llama_shape_sampled_rows():
+    B, L, h_q, g, d, W = 2, 2048, 32, 8, 128, 512
+    q = rand_bf16((B, L, h_q, d), 501)
+    k = rand_bf16((B, L, g, d), 502)
+    v = rand_bf16((B, L, g, d), 503)
+    scale = 1.0 / math.sqrt(d)
+    slopes = alibi_slopes(h_q)
+    o = gqa.gqa_prefill_fwd(q, k, v, causal=True, scale=scale, window=W, alibi_slopes=slopes)
+    torch.cuda.synchronize()
+    sl = slopes.cpu().numpy().astype(np.float64)
+    rng = np.random.default_rng(7)
+    for b, pos in [(0, 0), (1, L - 1), (0, W - 1), (1, W)] + [
+            (int(rng.integers(B)), int(rng.integers(L))) for _ in range(8)]:
+        lo = max(0, pos - W + 1)
+        o_r, _ = oracle.prefill(f64(q[b:b + 1, pos:pos + 1]), f64(k[b:b + 1, lo:pos + 1]),
+                                f64(v[b:b + 1, lo:pos + 1]), True, scale, q_offset=pos - lo,
+                                alibi_slopes=sl)
+        assert_close(f64(o[b, pos]), o_r[0, 0], f"row {pos} of batch {b}")
+
+
+def test_prefill_window_wider_than_sequence_equals_plain_causal():
+    B, L, h_q, g, d = 1, 333, 8, 4, 64
+    q, k, v = rand_bf16((B, L, h_q, d), 511), rand_bf16((B, L, g, d), 512), rand_bf16(
+        (B, L, g, d), 513)
+    a = gqa.gqa_prefill_fwd(q, k, v, causal=True, window=L)
+    b = gqa.gqa_prefill_fwd(q, k, v, causal=True)
+    torch.cuda.synchronize()
+    assert torch.equal(a, b)
+
+
+# ---------------------------------------------------------------------------
+# chunked prefill over the KV cache
+# ---------------------------------------------------------------------------
+
+def _cached_case(B, T, h_q, g, d, S_max, lens, seed, window=0, alibi=False, nan_tail=True):
+    kc = rand_bf16((B, g, S_max, d), seed)
+    vc = rand_bf16((B, g, S_max, d), seed + 1)
+    q = rand_bf16((B, T, h_q, d), seed + 2)
+    lens_t = torch.tensor(lens, dtype=torch.int32, device=DEV)
+    if nan_tail:
+        for b, n in enumerate(lens):
+            kc[b, :, n:] = float("nan")
+            vc[b, :, n:] = float("nan")
+    slopes = alibi_slopes(h_q) if alibi else None
+    scale = 1.0 / math.sqrt(d)
+    lse = torch.empty((B, h_q, T), dtype=torch.float32, device=DEV)
+    status = torch.zeros(1, dtype=torch.int32, device=DEV)
+    o = gqa.gqa_prefill_kvcache_fwd(q, kc, vc, lens_t, scale=scale, lse=lse, window=window,
+                                    alibi_slopes=slopes, status=status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    sl = None if slopes is None else slopes.cpu().numpy().astype(np.float64)
+    kc64 = np.nan_to_num(f64(kc))  # rows past the length are never visible to the oracle
+    vc64 = np.nan_to_num(f64(vc))
+    o_ref, lse_ref = oracle.prefill_cached(f64(q), kc64, vc64, lens, scale, window=window,
+                                           alibi_slopes=sl)
+    return o, lse, o_ref, lse_ref
+
+
+@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("T,lens", [(1, [1, 700, 1024]), (7, [7, 130, 999]),
+                                    (64, [64, 600, 1000]), (129, [129, 300, 1024]),
+                                    (300, [1024, 300, 777])])
+def test_prefill_kvcache_ragged(d, T, lens):
+    o, lse, o_ref, lse_ref = _cached_case(3, T, 32, 8, d, 1024, lens, seed=600 + T + d)
+    assert_close(f64(o), o_ref, f"kvcache T={T} d={d}")
+    assert_close(f64(lse), lse_ref, "lse")
+
+
+@pytest.mark.parametrize("h_q,g", [(8, 8), (32, 1), (16, 4)])
+@pytest.mark.parametrize("window,alibi", [(0, True), (96, False), (200, True)])
+def test_prefill_kvcache_variants(h_q, g, window, alibi):
+    o, lse, o_ref, lse_ref = _cached_case(2, 100, h_q, g, 128, 900, [900, 333], seed=700 + h_q,
+                                          window=window, alibi=alibi)
+    assert_close(f64(o), o_ref, f"kvcache window={window} alibi={alibi}")
+    assert_close(f64(lse), lse_ref, "lse", max_abs=2e-2)
+
+
+def test_append_then_chunked_prefill_then_decode_pipeline():
+    """Prompt prefill, a chunk appended and prefilled against the cache, then
+    a decode token: the path a serving loop runs, each step against the oracle."""
+    B, h_q, g, d, S_max, P, T = 2, 32, 8, 128, 512, 200, 48
+    kc = torch.zeros((B, g, S_max, d), dtype=torch.bfloat16, device=DEV)
+    vc = torch.zeros_like(kc)
+    lens = torch.zeros((B,), dtype=torch.int32, device=DEV)
+    status = torch.zeros(1, dtype=torch.int32, device=DEV)
+    k_all = rand_bf16((B, P + T + 1, g, d), 801)
+    v_all = rand_bf16((B, P + T + 1, g, d), 802)
+    q_all = rand_bf16((B, P + T + 1, h_q, d), 803)
+    gqa.kv_cache_append(kc, vc, lens, k_all[:, :P].contiguous(), v_all[:, :P].contiguous(),
+                        status=status)
+    gqa.kv_cache_append(kc, vc, lens, k_all[:, P:P + T].contiguous(),
+                        v_all[:, P:P + T].contiguous(), status=status)
+    o_chunk = gqa.gqa_prefill_kvcache_fwd(q_all[:, P:P + T].contiguous(), kc, vc, lens)
+    gqa.kv_cache_append(kc, vc, lens, k_all[:, P + T:].contiguous(), v_all[:, P + T:].contiguous(),
+                        status=status)
+    o_dec = gqa.gqa_decode_fwd(q_all[:, P + T].contiguous(), kc, vc, lens)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    o_full, _ = oracle.prefill(f64(q_all), f64(k_all), f64(v_all), True, 1.0 / math.sqrt(d))
+    assert_close(f64(o_chunk), o_full[:, P:P + T], "chunk rows")
+    assert_close(f64(o_dec), o_full[:, P + T], "decode row")
+
+
+def test_kvcache_bad_length_is_flagged():
+    B, T, h_q, g, d, S_max = 2, 16, 8, 2, 64, 256
+    kc = rand_bf16((B, g, S_max, d), 901)
+    vc = rand_bf16((B, g, S_max, d), 902)
+    q = rand_bf16((B, T, h_q, d), 903)
+    lens = torch.tensor([8, 100], dtype=torch.int32, device=DEV)  # 8 < T
+    status = torch.zeros(1, dtype=torch.int32, device=DEV)
+    gqa.gqa_prefill_kvcache_fwd(q, kc, vc, lens, status=status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == gqa.GQA_ERR_BAD_LENGTH
+
+
+# ---------------------------------------------------------------------------
+# decode: sliding window and ALiBi
+# ---------------------------------------------------------------------------
+
+@pytest.mark.parametrize("G_cfg", [(32, 8), (32, 1), (8, 8)])
+@pytest.mark.parametrize("window,alibi", [(1, False), (300, False), (0, True), (1000, True)])
+def test_decode_window_alibi(G_cfg, window, alibi):
+    h_q, g = G_cfg
+    B, d, S_max = 4, 128, 3000
+    kc = rand_bf16((B, g, S_max, d), 1000 + window)
+    vc = rand_bf16((B, g, S_max, d), 1001 + window)
+    q = rand_bf16((B, h_q, d), 1002 + window)
+    lens_l = [3000, 1, 299, 1777]
+    lens = torch.tensor(lens_l, dtype=torch.int32, device=DEV)
+    if window > 0:
+        # rows before the window must never be read
+        for b, n in enumerate(lens_l):
+            lo = max(0, n - window)
+            kc[b, :, :lo] = float("nan")
+            vc[b, :, :lo] = float("nan")
+    slopes = alibi_slopes(h_q) if alibi else None
+    lse = torch.empty((B, h_q), dtype=torch.float32, device=DEV)
+    status = torch.zeros(1, dtype=torch.int32, device=DEV)
+    o = gqa.gqa_decode_fwd(q, kc, vc, lens, scale=0.0884, lse=lse, window=window,
+                           alibi_slopes=slopes, status=status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    sl = None if slopes is None else slopes.cpu().numpy().astype(np.float64)
+    o_ref, lse_ref = oracle.decode(f64(q), np.nan_to_num(f64(kc)), np.nan_to_num(f64(vc)),
+                                   lens_l, 0.0884, window=window, alibi_slopes=sl)
+    assert_close(f64(o), o_ref, f"decode window={window} alibi={alibi}")
+    assert_close(f64(lse), lse_ref, "lse", max_abs=2e-2)
+
+
+def test_decode_equals_one_token_chunked_prefill_with_bias():
+    B, h_q, g, d, S_max = 3, 32, 8, 128, 1500
+    kc = rand_bf16((B, g, S_max, d), 1101)
+    vc = rand_bf16((B, g, S_max, d), 1102)
+    q = rand_bf16((B, h_q, d), 1103)
+    lens = torch.tensor([1500, 17, 640], dtype=torch.int32, device=DEV)
+    slopes = alibi_slopes(h_q)
+    o_d = gqa.gqa_decode_fwd(q, kc, vc, lens, window=400, alibi_slopes=slopes)
+    o_p = gqa.gqa_prefill_kvcache_fwd(q[:, None].contiguous(), kc, vc, lens, window=400,
+                                      alibi_slopes=slopes)
+    torch.cuda.synchronize()
+    assert_close(f64(o_d), f64(o_p[:, 0]), "decode vs one-token chunk", max_abs=5e-3)
