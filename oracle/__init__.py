@@ -16,4 +16,7 @@ from .gqa_oracle import (  # noqa: F401
     prefill_cached,
     decode,
     append,
+    gather_paged,
+    decode_paged,
+    append_paged,
 )

@@ -30,6 +30,11 @@ What it computes, and where the pages define it
 * Chunked prefill against a KV cache: new query tokens attend to the cached
   rows and, causally, to each other (the cache concatenation of the ijyty.com
   explainer, section 3.2, applied to more than one new token).
+* Paged KV cache with group-aligned pages (the jsqmd.com survey, section 4.3,
+  on PagedAttention: a page holds page_size tokens of one K/V group, and the
+  pages of the g groups of one block sit next to each other): a pool
+  ``[num_pages, g, page_size, d]`` and a per-sequence block table whose entry
+  ``i`` is the physical page of logical rows ``i*page_size .. (i+1)*page_size-1``.
 
 Readings where the pages are silent (each listed in the design notes):
 * causal mask: key ``j`` is visible to query ``i`` iff ``j <= i + q_offset``
@@ -315,3 +320,65 @@ def append(k_cache, v_cache, seq_lens, k_new, v_new):
                 vc[b, h, pos, :] = v_new[b, t, h, :]
         new_lens[b] = min(int(lens[b]) + T, S_max)
     return kc, vc, new_lens, status
+
+
+# ---------------------------------------------------------------------------
+# Paged KV cache
+# ---------------------------------------------------------------------------
+
+def gather_paged(pool, block_table, seq_lens, page_size: int):
+    """Contiguous ``[B, g, S, d]`` copy of a paged cache, S = blocks * page_size.
+
+    Logical row ``j`` of sequence ``b`` is row ``j % page_size`` of physical
+    page ``block_table[b][j // page_size]`` (of every K/V head). Rows at or
+    past ``seq_lens[b]`` are filled with zeros (they are never visible).
+    """
+    pool = np.asarray(pool)
+    table = np.asarray(block_table)
+    B, n_blocks = table.shape
+    g, d = pool.shape[1], pool.shape[3]
+    out = np.zeros((B, g, n_blocks * page_size, d), dtype=pool.dtype)
+    for b in range(B):
+        for j in range(int(seq_lens[b])):
+            page = int(table[b, j // page_size])
+            out[b, :, j, :] = pool[page, :, j % page_size, :]
+    return out
+
+
+def decode_paged(q, k_pool, v_pool, block_table, seq_lens, page_size: int, scale: float,
+                 window: int = 0, alibi_slopes=None):
+    """One-token GQA decode over a paged cache: the decode of the gathered rows."""
+    kc = gather_paged(k_pool, block_table, seq_lens, page_size)
+    vc = gather_paged(v_pool, block_table, seq_lens, page_size)
+    return decode(q, kc, vc, seq_lens, scale, window=window, alibi_slopes=alibi_slopes)
+
+
+def append_paged(k_pool, v_pool, block_table, seq_lens, k_new, v_new, page_size: int):
+    """``append`` for a paged cache: token ``t`` of sequence ``b`` goes to logical
+    row ``seq_lens[b] + t``, i.e. row ``(seq_lens[b] + t) % page_size`` of page
+    ``block_table[b][(seq_lens[b] + t) // page_size]``; rows past the table's
+    capacity are dropped and reported as APPEND_CACHE_FULL.
+    Returns (k_pool', v_pool', seq_lens', status).
+    """
+    kp = np.array(k_pool, copy=True)
+    vp = np.array(v_pool, copy=True)
+    table = np.asarray(block_table)
+    lens = np.array(seq_lens, copy=True).astype(np.int64)
+    B, n_blocks = table.shape
+    cap = n_blocks * page_size
+    g = kp.shape[1]
+    T = k_new.shape[1]
+    status = APPEND_OK
+    new_lens = lens.copy()
+    for b in range(B):
+        for t in range(T):
+            pos = int(lens[b]) + t
+            if pos >= cap:
+                status = APPEND_CACHE_FULL
+                continue
+            page = int(table[b, pos // page_size])
+            for h in range(g):
+                kp[page, h, pos % page_size, :] = k_new[b, t, h, :]
+                vp[page, h, pos % page_size, :] = v_new[b, t, h, :]
+        new_lens[b] = min(int(lens[b]) + T, cap)
+    return kp, vp, new_lens, status

@@ -532,3 +532,65 @@ def test_decode_window_equals_decode_over_the_last_rows():
         o_t, _ = oracle.decode(q[b:b + 1], kc[b:b + 1, :, n - W:n], vc[b:b + 1, :, n - W:n],
                                [W], 0.5, alibi_slopes=slopes)
         np.testing.assert_allclose(o[b], o_t[0], rtol=0, atol=1e-12)
+
+
+# ---------------------------------------------------------------------------
+# Paged KV cache
+# ---------------------------------------------------------------------------
+
+def _paged_from_contiguous(kc, page_size, perm_seed=None):
+    """Split a contiguous [B, g, S, d] cache into pages; optionally shuffle them."""
+    B, g, S, d = kc.shape
+    nb = S // page_size
+    # page b*nb + i holds rows i*page_size .. of sequence b (reshape, no loops)
+    pool = kc.reshape(B, g, nb, page_size, d).transpose(0, 2, 1, 3, 4).reshape(B * nb, g,
+                                                                                page_size, d)
+    table = np.arange(B * nb).reshape(B, nb)
+    if perm_seed is not None:
+        perm = np.random.default_rng(perm_seed).permutation(B * nb)
+        new_pool = np.empty_like(pool)
+        new_pool[perm] = pool          # page p moves to slot perm[p]
+        pool, table = new_pool, perm[table]
+    return pool, table
+
+
+def test_paged_decode_with_identity_table_equals_contiguous_decode():
+    B, h_q, g, d, S, P = 3, 8, 2, 8, 64, 16
+    kc, vc, q = _rand((B, g, S, d), 131), _rand((B, g, S, d), 132), _rand((B, h_q, d), 133)
+    lens = [64, 17, 1]
+    kp, table = _paged_from_contiguous(kc, P)
+    vp, _ = _paged_from_contiguous(vc, P)
+    o, lse = oracle.decode_paged(q, kp, vp, table, lens, P, 0.3)
+    o_c, lse_c = oracle.decode(q, kc, vc, lens, 0.3)
+    np.testing.assert_array_equal(o, o_c)
+    np.testing.assert_array_equal(lse, lse_c)
+
+
+def test_paged_decode_is_invariant_to_page_placement():
+    B, h_q, g, d, S, P = 2, 4, 4, 8, 48, 16
+    kc, vc, q = _rand((B, g, S, d), 141), _rand((B, g, S, d), 142), _rand((B, h_q, d), 143)
+    lens = [40, 48]
+    slopes = np.array([0.5, 0.25, 0.125, 0.0625])
+    kp, table = _paged_from_contiguous(kc, P, perm_seed=7)
+    vp, table_v = _paged_from_contiguous(vc, P, perm_seed=7)
+    assert np.array_equal(table, table_v)
+    for window, al in ((0, None), (20, slopes)):
+        o, _ = oracle.decode_paged(q, kp, vp, table, lens, P, 0.3, window=window,
+                                   alibi_slopes=al)
+        o_c, _ = oracle.decode(q, kc, vc, lens, 0.3, window=window, alibi_slopes=al)
+        np.testing.assert_array_equal(o, o_c)
+
+
+def test_paged_append_matches_contiguous_append():
+    B, g, d, S, P, T = 2, 2, 4, 32, 8, 5
+    kc, vc = _rand((B, g, S, d), 151), _rand((B, g, S, d), 152)
+    kn, vn = _rand((B, T, g, d), 153), _rand((B, T, g, d), 154)
+    lens = np.array([30, 6])  # sequence 0 overflows its 32-row capacity
+    kp, table = _paged_from_contiguous(kc, P, perm_seed=3)
+    vp, _ = _paged_from_contiguous(vc, P, perm_seed=3)
+    kp2, vp2, lens_p, st_p = oracle.append_paged(kp, vp, table, lens, kn, vn, P)
+    kc2, vc2, lens_c, st_c = oracle.append(kc, vc, lens, kn, vn)
+    assert st_p == st_c == oracle.APPEND_CACHE_FULL
+    assert list(lens_p) == list(lens_c) == [32, 11]
+    np.testing.assert_array_equal(oracle.gather_paged(kp2, table, lens_p, P), kc2 * (
+        np.arange(S)[None, None, :, None] < lens_c[:, None, None, None]))
