@@ -28,6 +28,7 @@ GQA_ERR_CUDA = 6
 GQA_ERR_TIMEOUT = 7
 GQA_ERR_BAD_LENGTH = 8
 GQA_ERR_SCRATCH_LIMIT = 9
+GQA_ERR_BAD_PAGE = 10
 GQA_OUT_F32 = 0
 GQA_OUT_BF16 = 1
 
@@ -67,6 +68,14 @@ def load_library() -> ctypes.CDLL:
     lib.gqa_decode_fwd_ex.argtypes = [vp, vp, vp, vp, vp, i32, vp, i32, i32, i32, i32, i32, f32,
                                       i32, vp, vp, sz, vp, vp]
     lib.gqa_decode_fwd_ex.restype = i32
+    lib.gqa_decode_paged_workspace_bytes.argtypes = [i32] * 6
+    lib.gqa_decode_paged_workspace_bytes.restype = sz
+    lib.gqa_decode_paged_fwd.argtypes = [vp, vp, vp, vp, vp, vp, i32, vp, i32, i32, i32, i32,
+                                         i32, i32, i32, f32, i32, vp, vp, sz, vp, vp]
+    lib.gqa_decode_paged_fwd.restype = i32
+    lib.kv_cache_append_paged.argtypes = [vp, vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, i32,
+                                          i32, vp, vp]
+    lib.kv_cache_append_paged.restype = i32
     lib.gqa_decode_workspace_bytes.argtypes = [i32, i32, i32, i32, i32]
     lib.gqa_decode_workspace_bytes.restype = sz
     lib.gqa_decode_fwd.argtypes = [vp, vp, vp, vp, vp, i32, vp, i32, i32, i32, i32, i32, f32,
@@ -299,3 +308,77 @@ def kv_cache_append(k_cache: torch.Tensor, v_cache: torch.Tensor, seq_lens: torc
                              _stream_ptr(stream, k_cache.device))
     if rc != GQA_OK:
         raise GQAError(rc, "kv_cache_append")
+
+
+def gqa_decode_paged_workspace_bytes(B: int, h_q: int, g: int, d: int, page_size: int,
+                                     max_blocks: int) -> int:
+    return int(load_library().gqa_decode_paged_workspace_bytes(B, h_q, g, d, page_size,
+                                                               max_blocks))
+
+
+def gqa_decode_paged_fwd(q: torch.Tensor, k_pool: torch.Tensor, v_pool: torch.Tensor,
+                         block_table: torch.Tensor, seq_lens: torch.Tensor, *,
+                         scale: Optional[float] = None, out: Optional[torch.Tensor] = None,
+                         out_dtype=torch.float32, lse: Optional[torch.Tensor] = None,
+                         window: int = 0, alibi_slopes: Optional[torch.Tensor] = None,
+                         workspace: Optional[torch.Tensor] = None,
+                         status: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
+    """Decode over a paged cache: pools [num_pages, g, page_size, d], block_table
+    [B, max_blocks] int32 (physical page of each logical block) -> out [B, h_q, d]."""
+    lib = load_library()
+    B, h_q, d = q.shape
+    num_pages, g, page_size = k_pool.shape[0], k_pool.shape[1], k_pool.shape[2]
+    max_blocks = block_table.shape[1]
+    _check(q, "q", torch.bfloat16)
+    _check(k_pool, "k_pool", torch.bfloat16, (num_pages, g, page_size, d))
+    _check(v_pool, "v_pool", torch.bfloat16, (num_pages, g, page_size, d))
+    _check(block_table, "block_table", torch.int32, (B, max_blocks))
+    _check(seq_lens, "seq_lens", torch.int32, (B,))
+    if out is None:
+        out = torch.empty((B, h_q, d), dtype=out_dtype, device=q.device)
+    _check(out, "out", out.dtype, (B, h_q, d))
+    if lse is not None:
+        _check(lse, "lse", torch.float32, (B, h_q))
+    if status is not None:
+        _check(status, "status", torch.int32)
+    _check_slopes(alibi_slopes, h_q)
+    need = gqa_decode_paged_workspace_bytes(B, h_q, g, d, page_size, max_blocks)
+    if workspace is None:
+        workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=q.device)
+    _check(workspace, "workspace", torch.uint8)
+    if scale is None:
+        scale = 1.0 / (d ** 0.5)
+    rc = lib.gqa_decode_paged_fwd(_ptr(q), _ptr(k_pool), _ptr(v_pool), _ptr(block_table),
+                                  _ptr(seq_lens), _ptr(out), _out_code(out.dtype), _ptr(lse), B,
+                                  h_q, g, d, page_size, num_pages, max_blocks, float(scale),
+                                  int(window), _ptr(alibi_slopes), _ptr(workspace),
+                                  workspace.numel(), _ptr(status),
+                                  _stream_ptr(stream, q.device))
+    if rc != GQA_OK:
+        raise GQAError(rc, "gqa_decode_paged_fwd")
+    return out
+
+
+def kv_cache_append_paged(k_pool: torch.Tensor, v_pool: torch.Tensor,
+                          block_table: torch.Tensor, seq_lens: torch.Tensor,
+                          k_new: torch.Tensor, v_new: torch.Tensor, *,
+                          status: Optional[torch.Tensor] = None, stream=None) -> None:
+    """Append k_new/v_new [B,T,g,d] through the block table; advances seq_lens."""
+    lib = load_library()
+    num_pages, g, page_size, d = k_pool.shape
+    B, max_blocks = block_table.shape
+    T = k_new.shape[1]
+    _check(k_pool, "k_pool", torch.bfloat16)
+    _check(v_pool, "v_pool", torch.bfloat16, (num_pages, g, page_size, d))
+    _check(block_table, "block_table", torch.int32, (B, max_blocks))
+    _check(seq_lens, "seq_lens", torch.int32, (B,))
+    _check(k_new, "k_new", torch.bfloat16, (B, T, g, d))
+    _check(v_new, "v_new", torch.bfloat16, (B, T, g, d))
+    if status is not None:
+        _check(status, "status", torch.int32)
+    rc = lib.kv_cache_append_paged(_ptr(k_pool), _ptr(v_pool), _ptr(block_table),
+                                   _ptr(seq_lens), _ptr(k_new), _ptr(v_new), B, g, d, page_size,
+                                   num_pages, max_blocks, T, _ptr(status),
+                                   _stream_ptr(stream, k_pool.device))
+    if rc != GQA_OK:
+        raise GQAError(rc, "kv_cache_append_paged")

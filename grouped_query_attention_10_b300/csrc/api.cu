@@ -98,6 +98,20 @@ bool decode_shape_ok(int B, int h_q, int g, int d, int S_max) {
   return true;
 }
 
+// Pages of 16 .. 65536 tokens (a power of two); the logical capacity
+// page_size * max_blocks must fit an int.
+bool paged_ok(int page_size, int max_blocks) {
+  return page_size >= 16 && page_size <= 65536 && pow2(page_size) && max_blocks >= 1 &&
+         static_cast<long long>(page_size) * max_blocks < (1LL << 31);
+}
+
+int decode_common(const void* q, const void* k_cache, const void* v_cache,
+                  const int32_t* seq_lens, const int32_t* block_table, int page_size,
+                  int num_pages, int max_blocks, void* o, int o_dtype, float* lse, int B,
+                  int h_q, int g, int d, int S_max, float scale, int window,
+                  const float* alibi_slopes, void* workspace, size_t workspace_bytes,
+                  int32_t* status_dev, void* stream);
+
 }  // namespace
 
 extern "C" {
@@ -115,6 +129,7 @@ const char* gqa_status_string(int status) {
     case GQA_ERR_BAD_LENGTH: return "GQA_ERR_BAD_LENGTH: a sequence length was out of range";
     case GQA_ERR_SCRATCH_LIMIT:
       return "GQA_ERR_SCRATCH_LIMIT: sizes need more than the built-in decode scratch";
+    case GQA_ERR_BAD_PAGE: return "GQA_ERR_BAD_PAGE: a block-table entry in use was outside the pool";
     default: return "GQA_ERR_UNKNOWN";
   }
 }
@@ -260,6 +275,44 @@ int gqa_decode_fwd_ex(const void* q, const void* k_cache, const void* v_cache,
                       int g, int d, int S_max, float scale, int window,
                       const float* alibi_slopes, void* workspace, size_t workspace_bytes,
                       int32_t* status_dev, void* stream) {
+  return decode_common(q, k_cache, v_cache, seq_lens, nullptr, 0, 0, 0, o, o_dtype, lse, B, h_q,
+                       g, d, S_max, scale, window, alibi_slopes, workspace, workspace_bytes,
+                       status_dev, stream);
+}
+
+size_t gqa_decode_paged_workspace_bytes(int B, int h_q, int g, int d, int page_size,
+                                        int max_blocks) {
+  if (!paged_ok(page_size, max_blocks)) return 0;
+  return gqa_decode_workspace_bytes(B, h_q, g, d, page_size * max_blocks);
+}
+
+int gqa_decode_paged_fwd(const void* q, const void* k_pool, const void* v_pool,
+                         const int32_t* block_table, const int32_t* seq_lens, void* o,
+                         int o_dtype, float* lse, int B, int h_q, int g, int d, int page_size,
+                         int num_pages, int max_blocks, float scale, int window,
+                         const float* alibi_slopes, void* workspace, size_t workspace_bytes,
+                         int32_t* status_dev, void* stream) {
+  if (block_table == nullptr) return GQA_ERR_NULL;
+  if (!paged_ok(page_size, max_blocks) || num_pages < 1 ||
+      static_cast<long long>(num_pages) * g * page_size * d >= kMaxElems ||
+      static_cast<long long>(num_pages) * g >= (1LL << 31))
+    return GQA_ERR_SHAPE;
+  if (!aligned4(block_table)) return GQA_ERR_ALIGN;
+  return decode_common(q, k_pool, v_pool, seq_lens, block_table, page_size, num_pages,
+                       max_blocks, o, o_dtype, lse, B, h_q, g, d, page_size * max_blocks, scale,
+                       window, alibi_slopes, workspace, workspace_bytes, status_dev, stream);
+}
+
+}  // extern "C"
+
+namespace {
+
+int decode_common(const void* q, const void* k_cache, const void* v_cache,
+                  const int32_t* seq_lens, const int32_t* block_table, int page_size,
+                  int num_pages, int max_blocks, void* o, int o_dtype, float* lse, int B,
+                  int h_q, int g, int d, int S_max, float scale, int window,
+                  const float* alibi_slopes, void* workspace, size_t workspace_bytes,
+                  int32_t* status_dev, void* stream) {
   if (q == nullptr || k_cache == nullptr || v_cache == nullptr || seq_lens == nullptr ||
       o == nullptr)
     return GQA_ERR_NULL;
@@ -277,12 +330,29 @@ int gqa_decode_fwd_ex(const void* q, const void* k_cache, const void* v_cache,
 
   gqa::DecodeArgs a{};
   const cuuint64_t e = 2;
-  const cuuint64_t dims[3] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(S_max),
-                              static_cast<cuuint64_t>(B) * g};
-  const cuuint64_t strides[2] = {d * e, static_cast<cuuint64_t>(S_max) * d * e};
-  const cuuint32_t box[3] = {64, static_cast<cuuint32_t>(gqa::kDecodeStage), 1};
-  if (!encode_bf16(&a.tm_k, 3, k_cache, dims, strides, box)) return GQA_ERR_CUDA;
-  if (!encode_bf16(&a.tm_v, 3, v_cache, dims, strides, box)) return GQA_ERR_CUDA;
+  if (block_table == nullptr) {
+    const cuuint64_t dims[3] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(S_max),
+                                static_cast<cuuint64_t>(B) * g};
+    const cuuint64_t strides[2] = {d * e, static_cast<cuuint64_t>(S_max) * d * e};
+    const cuuint32_t box[3] = {64, static_cast<cuuint32_t>(gqa::kDecodeStage), 1};
+    if (!encode_bf16(&a.tm_k, 3, k_cache, dims, strides, box)) return GQA_ERR_CUDA;
+    if (!encode_bf16(&a.tm_v, 3, v_cache, dims, strides, box)) return GQA_ERR_CUDA;
+  } else {
+    // pool [num_pages, g, page_size, d]: map {d, page_size, num_pages * g}; a box
+    // is one page's rows, at most one 64-token stage
+    const cuuint64_t dims[3] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(page_size),
+                                static_cast<cuuint64_t>(num_pages) * g};
+    const cuuint64_t strides[2] = {d * e, static_cast<cuuint64_t>(page_size) * d * e};
+    const cuuint32_t rows = static_cast<cuuint32_t>(
+        page_size < gqa::kDecodeStage ? page_size : gqa::kDecodeStage);
+    const cuuint32_t box[3] = {64, rows, 1};
+    if (!encode_bf16(&a.tm_k, 3, k_cache, dims, strides, box)) return GQA_ERR_CUDA;
+    if (!encode_bf16(&a.tm_v, 3, v_cache, dims, strides, box)) return GQA_ERR_CUDA;
+  }
+  a.block_table = block_table;
+  a.page_log2 = block_table == nullptr ? 0 : log2i(page_size);
+  a.num_pages = num_pages;
+  a.max_blocks = max_blocks;
   a.q = q;
   a.seq_lens = seq_lens;
   a.o = o;
@@ -305,6 +375,36 @@ int gqa_decode_fwd_ex(const void* q, const void* k_cache, const void* v_cache,
   a.status = status_dev;
   return gqa::launch_decode(a, static_cast<cudaStream_t>(stream)) == cudaSuccess ? GQA_OK
                                                                                    : GQA_ERR_CUDA;
+}
+
+}  // namespace
+
+extern "C" {
+
+int kv_cache_append_paged(void* k_pool, void* v_pool, const int32_t* block_table,
+                          int32_t* seq_lens, const void* k_new, const void* v_new, int B, int g,
+                          int d, int page_size, int num_pages, int max_blocks, int T,
+                          int32_t* status_dev, void* stream) {
+  if (k_pool == nullptr || v_pool == nullptr || block_table == nullptr || seq_lens == nullptr ||
+      k_new == nullptr || v_new == nullptr)
+    return GQA_ERR_NULL;
+  if (B < 1 || g < 1 || (d != 64 && d != 128) || T < 0 || num_pages < 1 ||
+      !paged_ok(page_size, max_blocks))
+    return GQA_ERR_SHAPE;
+  if (static_cast<long long>(num_pages) * g * page_size * d >= kMaxElems ||
+      static_cast<long long>(B) * T * g * d >= kMaxElems ||
+      static_cast<long long>(B) * max_blocks >= (1LL << 31))
+    return GQA_ERR_SHAPE;
+  if (!aligned16(k_pool) || !aligned16(v_pool) || !aligned16(k_new) || !aligned16(v_new) ||
+      !aligned4(seq_lens) || !aligned4(block_table))
+    return GQA_ERR_ALIGN;
+  if (status_dev != nullptr && !aligned4(status_dev)) return GQA_ERR_ALIGN;
+  if (T == 0) return GQA_OK;
+  return gqa::launch_append_paged(k_pool, v_pool, block_table, seq_lens, k_new, v_new, B, g, d,
+                                  log2i(page_size), num_pages, max_blocks, T, status_dev,
+                                  static_cast<cudaStream_t>(stream)) == cudaSuccess
+             ? GQA_OK
+             : GQA_ERR_CUDA;
 }
 
 int kv_cache_append(void* k_cache, void* v_cache, int32_t* seq_lens, const void* k_new,

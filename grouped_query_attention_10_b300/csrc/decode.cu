@@ -74,6 +74,7 @@ __device__ __forceinline__ uint32_t sw128(int row, int chunk) {
 struct Item {
   int b, kvh, hs, split;
   int len;           // valid rows of the sequence (the query sits at len - 1)
+  int lo;            // first row inside the sliding window (0 without one)
   int s0, s1, n_st;  // token range [s0, s1) and its 64-token stages (0: nothing to do)
 };
 
@@ -93,9 +94,11 @@ __device__ __forceinline__ Item decode_item(int u, const int32_t* seq_lens, int 
   int len = seq_lens[it.b];
   len = len < 0 ? 0 : (len > S_max ? S_max : len);
   it.len = len;
-  // rows before the sliding window (if any) are not read at all
-  const int lo = window > 0 ? max(0, len - window) : 0;
-  it.s0 = max(it.split * split_len, lo);
+  // rows before the sliding window's 64-row stage are not read at all; the
+  // stage start stays a multiple of 64 (of the split length too), so a paged
+  // stage never begins inside a page, and the rows in [s0, lo) are masked
+  it.lo = window > 0 ? max(0, len - window) : 0;
+  it.s0 = max(it.split * split_len, it.lo & ~(kDecodeStage - 1));
   it.s1 = min(len, it.split * split_len + split_len);
   it.n_st = it.s0 < it.s1 ? (it.s1 - it.s0 + kDecodeStage - 1) / kDecodeStage : 0;
   return it;
@@ -110,7 +113,8 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) decode_split_kernel(
     const __nv_bfloat16* __restrict__ q, const int32_t* __restrict__ seq_lens,
     float* __restrict__ part_o, float* __restrict__ part_lse, int h_q, int g, int G,
     int n_hslice, int S_max, int split_len, int n_split, int n_items, float scale_log2,
-    int window, const float* __restrict__ alibi, int* __restrict__ item_counter,
+    int window, const float* __restrict__ alibi, const int32_t* __restrict__ block_table,
+    int page_log2, int num_pages, int max_blocks, int* __restrict__ item_counter,
     int32_t* status) {
   using C = DecCfg<D>;
   constexpr int kStages = C::kStages;
@@ -162,11 +166,42 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) decode_split_kernel(
           uint8_t* base = smem + slot * C::kStageBytes;
           const int y = it.s0 + st * kDecodeStage;
           mbar_arrive_expect_tx(&full_bar[slot], C::kStageBytes);
+          if (block_table == nullptr) {
 #pragma unroll
-          for (int cb = 0; cb < kCB; ++cb) {
-            tma_load_3d(base + cb * C::kBoxBytes, &tm_k, &full_bar[slot], cb * 64, y, zrow);
-            tma_load_3d(base + (kCB + cb) * C::kBoxBytes, &tm_v, &full_bar[slot], cb * 64, y,
-                        zrow);
+            for (int cb = 0; cb < kCB; ++cb) {
+              tma_load_3d(base + cb * C::kBoxBytes, &tm_k, &full_bar[slot], cb * 64, y, zrow);
+              tma_load_3d(base + (kCB + cb) * C::kBoxBytes, &tm_v, &full_bar[slot], cb * 64, y,
+                          zrow);
+            }
+          } else {
+            // paged cache: the stage's 64 rows come from one page or from
+            // 64 / page_size consecutive logical blocks; a box lands at its
+            // row offset of the stage (a multiple of 16 rows, so the 128-byte
+            // swizzle of the whole stage is kept)
+            const int rows = min(kDecodeStage, 1 << page_log2);
+            for (int sub = 0; sub < kDecodeStage; sub += rows) {
+              const int tok = y + sub;
+              const int lb = tok >> page_log2;
+              int page = lb < max_blocks ? block_table[static_cast<size_t>(it.b) * max_blocks + lb]
+                                         : -1;
+              if (page < 0 || page >= num_pages) {
+                // an entry the sequence uses inside its window must name a
+                // page of the pool (pages wholly before the window may be
+                // gone); a missing page reads zeros (the load starts out of
+                // range)
+                if (tok < it.s1 && tok + rows > it.lo) record_status(status, GQA_ERR_BAD_PAGE);
+                page = -1;
+              }
+              const int zr = page < 0 ? -1 : page * g + it.kvh;
+              const int yr = tok & ((1 << page_log2) - 1);
+#pragma unroll
+              for (int cb = 0; cb < kCB; ++cb) {
+                tma_load_3d(base + cb * C::kBoxBytes + sub * 128, &tm_k, &full_bar[slot],
+                            cb * 64, yr, zr);
+                tma_load_3d(base + (kCB + cb) * C::kBoxBytes + sub * 128, &tm_v,
+                            &full_bar[slot], cb * 64, yr, zr);
+              }
+            }
           }
         }
       }
@@ -244,6 +279,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) decode_split_kernel(
       }
       const int tok0 = it.s0 + st * kDecodeStage;
       const int valid = it.s1 - tok0;  // rows of this stage that are real
+      const int first = it.lo - tok0;  // rows of this stage before the window
       const uint32_t kbase = smem_base + slot * C::kStageBytes;
       const uint32_t vbase = kbase + kCB * C::kBoxBytes;
       // This warp's 16-token blocks of the stage are processed together (their
@@ -255,16 +291,17 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) decode_split_kernel(
       for (int sb = 0; sb < kSubPerWarp; ++sb) {
         r0[sb] = (slice + sb * kNSlices) * 16;  // first row of the 16-token block
         act[sb] = r0[sb] < valid;               // any real token in it
-        if (act[sb] && r0[sb] + 16 > valid) {
-          // rows past the sequence may hold anything (even NaN) and 0 * NaN
-          // would poison P.V: zero this block's V rows past the end. Only the
-          // warps that read these rows write them, and all write zeros.
+        if (act[sb] && (r0[sb] + 16 > valid || r0[sb] < first)) {
+          // rows past the sequence or before the window may hold anything
+          // (even NaN) and 0 * NaN would poison P.V: zero this block's V rows
+          // there. Only the warps that read these rows write them, and all
+          // write zeros.
           uint8_t* vrows = smem + slot * C::kStageBytes + kCB * C::kBoxBytes;
           for (int i = lane; i < 16 * kCB * 8; i += 32) {
             const int r = r0[sb] + i / (kCB * 8);
             const int cb = (i / 8) % kCB;
             const int ch = i % 8;
-            if (r >= valid)
+            if (r >= valid || r < first)
               *reinterpret_cast<uint4*>(vrows + cb * C::kBoxBytes + r * 128 + ch * 16) =
                   make_uint4(0u, 0u, 0u, 0u);
           }
@@ -309,7 +346,8 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) decode_split_kernel(
               const float bias =
                   slope[e >> 1] * static_cast<float>(tok0 + tok - (it.len - 1));
               const float x =
-                  act[sb] && tok < valid ? fmaf(s[sb][j][e], scale_log2, bias) : -INFINITY;
+                  act[sb] && tok < valid && tok >= first ? fmaf(s[sb][j][e], scale_log2, bias)
+                                                         : -INFINITY;
               s[sb][j][e] = x;
               mx[e >> 1] = fmaxf(mx[e >> 1], x);
             }
@@ -580,7 +618,8 @@ static cudaError_t launch_decode_t(const DecodeArgs& a, cudaStream_t s) {
   decode_split_kernel<D, MT><<<grid, kThreads, kSmem, s>>>(
       a.tm_k, a.tm_v, static_cast<const __nv_bfloat16*>(a.q), a.seq_lens, a.part_o, a.part_lse,
       a.h_q, a.g, a.G, n_hslice, a.S_max, a.split_len, a.n_split, static_cast<int>(n_items),
-      a.scale_log2, a.window, a.alibi, a.item_counter, a.status);
+      a.scale_log2, a.window, a.alibi, a.block_table, a.page_log2, a.num_pages, a.max_blocks,
+      a.item_counter, a.status);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   decode_combine_kernel<D><<<a.B * a.h_q, kCombineThreads, 0, s>>>(a.part_o, a.part_lse, a.seq_lens, a.o,

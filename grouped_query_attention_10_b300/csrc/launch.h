@@ -47,6 +47,9 @@ struct DecodeArgs {
   float scale_log2;
   int window;          // sliding window (the last `window` rows), 0: none
   const float* alibi;  // per-query-head ALiBi slopes, or nullptr
+  // paged cache (block_table != nullptr): K/V maps are {d, page_size, num_pages*g}
+  const int32_t* block_table;  // [B, max_blocks] physical page of each logical block
+  int page_log2, num_pages, max_blocks;
   int32_t* status;
 };
 
@@ -55,6 +58,12 @@ cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t s);
 cudaError_t launch_append(void* k_cache, void* v_cache, int32_t* seq_lens, const void* k_new,
                           const void* v_new, int B, int g, int d, int S_max, int T,
                           int32_t* status, cudaStream_t s);
+// Paged variant: rows go through block_table [B, max_blocks] into a pool
+// [num_pages, g, 1 << page_log2, d].
+cudaError_t launch_append_paged(void* k_pool, void* v_pool, const int32_t* block_table,
+                                int32_t* seq_lens, const void* k_new, const void* v_new, int B,
+                                int g, int d, int page_log2, int num_pages, int max_blocks, int T,
+                                int32_t* status, cudaStream_t s);
 
 // Split length (tokens per split-KV CTA) used for these decode sizes.
 int decode_split_len(int B, int h_q, int g, int S_max);

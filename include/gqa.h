@@ -51,7 +51,8 @@ typedef enum {
   GQA_ERR_CUDA = 6,        /* a CUDA runtime call or a launch failed              */
   GQA_ERR_TIMEOUT = 7,     /* (device) a bounded wait inside a kernel ran out     */
   GQA_ERR_BAD_LENGTH = 8,  /* (device) a seq_lens entry was negative or > S_max   */
-  GQA_ERR_SCRATCH_LIMIT = 9 /* the sizes need more scratch than the built-in array */
+  GQA_ERR_SCRATCH_LIMIT = 9, /* the sizes need more scratch than the built-in array */
+  GQA_ERR_BAD_PAGE = 10     /* (device) a block-table entry in use was outside the pool */
 } gqa_status_t;
 
 typedef enum {
@@ -198,6 +199,51 @@ int gqa_decode_fwd_ex(const void* q, const void* k_cache, const void* v_cache,
 int kv_cache_append(void* k_cache, void* v_cache, int32_t* seq_lens,
                     const void* k_new, const void* v_new, int B, int g, int d,
                     int S_max, int T, int32_t* status_dev, void* stream);
+
+/*
+ * Paged KV cache with group-aligned pages (the PagedAttention integration of
+ * the jsqmd.com survey, section 4.3: a page holds page_size tokens of one K/V
+ * group, and the g group pages of one physical block are adjacent):
+ *
+ *   k_pool, v_pool  [num_pages, g, page_size, d] bf16
+ *   block_table     device int32 [B, max_blocks]; entry i of sequence b is the
+ *                   physical page of its logical rows i*page_size ..
+ *                   (i+1)*page_size - 1 (entries past a sequence's length are
+ *                   never read)
+ *   page_size       a power of two in [16, 65536]; the logical capacity of a
+ *                   sequence is page_size * max_blocks (< 2^31)
+ *
+ * An entry that is in use but outside [0, num_pages) reads zeros and is
+ * flagged GQA_ERR_BAD_PAGE; sizes out of range are GQA_ERR_SHAPE.
+ */
+
+/* Workspace of gqa_decode_paged_fwd (0 for sizes it would reject). */
+size_t gqa_decode_paged_workspace_bytes(int B, int h_q, int g, int d, int page_size,
+                                        int max_blocks);
+
+/*
+ * gqa_decode_paged_fwd -- gqa_decode_fwd_ex over a paged cache: the same
+ * result as gqa_decode_fwd_ex on the contiguous cache whose row j of
+ * sequence b is row j % page_size of page block_table[b][j / page_size].
+ * seq_lens entries are in [0, page_size * max_blocks].
+ */
+int gqa_decode_paged_fwd(const void* q, const void* k_pool, const void* v_pool,
+                         const int32_t* block_table, const int32_t* seq_lens, void* o,
+                         int o_dtype, float* lse, int B, int h_q, int g, int d, int page_size,
+                         int num_pages, int max_blocks, float scale, int window,
+                         const float* alibi_slopes, void* workspace, size_t workspace_bytes,
+                         int32_t* status_dev, void* stream);
+
+/*
+ * kv_cache_append_paged -- kv_cache_append into a paged cache: token t of
+ * sequence b goes to logical row seq_lens[b] + t through the block table.
+ * Rows past the capacity page_size * max_blocks are dropped and flagged
+ * GQA_ERR_CACHE_FULL; lengths saturate at the capacity. Two launches.
+ */
+int kv_cache_append_paged(void* k_pool, void* v_pool, const int32_t* block_table,
+                          int32_t* seq_lens, const void* k_new, const void* v_new, int B, int g,
+                          int d, int page_size, int num_pages, int max_blocks, int T,
+                          int32_t* status_dev, void* stream);
 
 /*
  * gqa_decode_fwd_noalloc -- gqa_decode_fwd for callers that cannot allocate.

@@ -48,7 +48,7 @@ def test_library_exports_every_declared_symbol(lib):
 
 def test_version_and_status_strings(lib):
     assert lib.gqa_version() == 100
-    for code in range(0, 9):
+    for code in range(0, 11):
         s = binding.status_string(code)
         assert s.startswith("GQA_")
     assert binding.status_string(99) == "GQA_ERR_UNKNOWN"
@@ -154,3 +154,27 @@ def test_variant_entry_points_validation(lib):
                                      alibi, f, ws, None, None)
     assert dec(window=-1) == binding.GQA_ERR_SHAPE
     assert dec(alibi=FAKE + 1) == binding.GQA_ERR_ALIGN
+
+
+def test_paged_entry_points_validation(lib):
+    f = FAKE
+    assert lib.gqa_decode_paged_workspace_bytes(4, 32, 8, 128, 16, 64) == \
+        lib.gqa_decode_workspace_bytes(4, 32, 8, 128, 1024)
+    assert lib.gqa_decode_paged_workspace_bytes(4, 32, 8, 128, 24, 64) == 0   # not a power of 2
+    assert lib.gqa_decode_paged_workspace_bytes(4, 32, 8, 128, 8, 64) == 0    # page too small
+    ws = lib.gqa_decode_paged_workspace_bytes(4, 32, 8, 128, 64, 16)
+
+    def dec(table=f, page=64, pages=100, blocks=16):
+        return lib.gqa_decode_paged_fwd(f, f, f, table, f, f, 0, None, 4, 32, 8, 128, page, pages,
+                                        blocks, 0.088, 0, None, f, ws, None, None)
+    assert dec(table=None) == binding.GQA_ERR_NULL
+    assert dec(page=48) == binding.GQA_ERR_SHAPE
+    assert dec(pages=0) == binding.GQA_ERR_SHAPE
+    assert dec(table=FAKE + 2) == binding.GQA_ERR_ALIGN
+
+    def app(table=f, page=64, T=1):
+        return lib.kv_cache_append_paged(f, f, table, f, f, f, 2, 8, 128, page, 10, 4, T, None,
+                                         None)
+    assert app(table=None) == binding.GQA_ERR_NULL
+    assert app(page=100) == binding.GQA_ERR_SHAPE
+    assert app(T=0) == binding.GQA_OK
