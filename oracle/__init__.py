@@ -19,4 +19,8 @@ from .gqa_oracle import (  # noqa: F401
     gather_paged,
     decode_paged,
     append_paged,
+    rope,
+    rope_f32,
+    append_rope,
+    append_paged_rope,
 )

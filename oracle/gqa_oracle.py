@@ -36,6 +36,15 @@ What it computes, and where the pages define it
   ``[num_pages, g, page_size, d]`` and a per-sequence block table whose entry
   ``i`` is the physical page of logical rows ``i*page_size .. (i+1)*page_size-1``.
 
+* Rotary position embedding (RoPE) of queries and keys: the pair
+  ``(x[2i], x[2i+1])`` of a row at position ``p`` is turned by the angle whose
+  cosine and sine are ``cos[p, i]`` and ``sin[p, i]``; the turned even parts
+  form the first half of the output row and the turned odd parts the second
+  half (the RoPE code of the jsqmd.com survey, chapter 1, whose cos/sin
+  tables of shape ``[seq_len, head_dim // 2]`` are inputs). Applied to the new
+  tokens' Q and K rows on their way into the cache, at the positions they
+  take there (the survey's fused-RoPE build option, chapter 5).
+
 Readings where the pages are silent (each listed in the design notes):
 * causal mask: key ``j`` is visible to query ``i`` iff ``j <= i + q_offset``
   (``q_offset = 0`` when queries and keys cover the same positions; a chunk
@@ -47,7 +56,13 @@ Readings where the pages are silent (each listed in the design notes):
 * a decode query sits at position ``seq_len - 1`` of its sequence;
 * dropout is the identity (inference);
 * a decode row with zero valid cache rows returns zeros and ``lse = -inf``;
-* ``append`` drops rows that would land past ``S_max`` and reports it.
+* ``append`` drops rows that would land past ``S_max`` and reports it;
+* RoPE precision: the survey's code multiplies bf16 rows by fp32 tables, so
+  the rotation is evaluated in binary32 (each product and the sum or
+  difference rounded to binary32, no fused multiply-add) and the result is
+  rounded to bf16 when it is stored; a new token ``t`` of sequence ``b`` sits
+  at position ``seq_lens[b] + t`` (the cache row it is written to), and query
+  rows of tokens dropped for lack of room are left unwritten.
 
 Everything here is the definition written out: one K/V duplication, one
 score matrix per (batch, head), one softmax, one product with V. No tiling,
@@ -382,3 +397,101 @@ def append_paged(k_pool, v_pool, block_table, seq_lens, k_new, v_new, page_size:
                 vp[page, h, pos % page_size, :] = v_new[b, t, h, :]
         new_lens[b] = min(int(lens[b]) + T, cap)
     return kp, vp, new_lens, status
+
+
+# ---------------------------------------------------------------------------
+# Rotary position embedding on the way into the cache
+# ---------------------------------------------------------------------------
+
+def rope(x, cos, sin, positions):
+    """The survey's rotary embedding in fp64 (jsqmd.com, chapter 1).
+
+    x: [..., n, d] rows; positions: [n] (or broadcastable) table rows;
+    cos, sin: [n_pos, d // 2]. Returns the rows with
+    ``out[..., i] = x[2i] cos - x[2i+1] sin`` and
+    ``out[..., d/2 + i] = x[2i] sin + x[2i+1] cos``.
+    """
+    x = np.asarray(x, dtype=np.float64)
+    c = np.asarray(cos, dtype=np.float64)[np.asarray(positions)]
+    s = np.asarray(sin, dtype=np.float64)[np.asarray(positions)]
+    even = x[..., 0::2]
+    odd = x[..., 1::2]
+    return np.concatenate([even * c - odd * s, even * s + odd * c], axis=-1)
+
+
+def rope_f32(x, cos, sin, positions):
+    """``rope`` as the survey's code evaluates it for bf16 rows and fp32
+    tables: every product, sum and difference rounded to binary32."""
+    x = np.asarray(x, dtype=np.float32)
+    c = np.asarray(cos, dtype=np.float32)[np.asarray(positions)]
+    s = np.asarray(sin, dtype=np.float32)[np.asarray(positions)]
+    even = x[..., 0::2]
+    odd = x[..., 1::2]
+    first = (even * c).astype(np.float32) - (odd * s).astype(np.float32)
+    second = (even * s).astype(np.float32) + (odd * c).astype(np.float32)
+    return np.concatenate([first, second], axis=-1).astype(np.float32)
+
+
+def _rope_new_rows(x_bits, cos, sin, seq_lens, capacity):
+    """Rotate rows ``[B, T, H, d]`` (bf16 bit patterns) of new tokens at their
+    cache positions ``seq_lens[b] + t``; rows at or past ``capacity`` (dropped)
+    are returned as given. Result: bf16 bit patterns."""
+    x_bits = np.asarray(x_bits).view(np.uint16)
+    out = x_bits.copy()
+    B, T = x_bits.shape[:2]
+    for b in range(B):
+        for t in range(T):
+            pos = int(seq_lens[b]) + t
+            if pos >= capacity:
+                continue
+            row = bf16_bits_to_f64(x_bits[b, t])  # [H, d], exact
+            out[b, t] = f32_to_bf16_bits(rope_f32(row, cos, sin, pos))
+    return out
+
+
+def append_rope(k_cache, v_cache, seq_lens, k_new, v_new, cos, sin, q=None, q_out=None):
+    """``append`` of RoPE-rotated keys, and the new tokens' queries rotated at
+    the same positions.
+
+    k_cache, v_cache, k_new, v_new, q, q_out: bf16 bit patterns (uint16 or
+    int16 views); q, q_out: [B, T, h_q, d]. Returns
+    (k_cache', v_cache', seq_lens', status, q_out') where q_out' is q_out
+    (a copy of q if q_out is None) with the rows of stored tokens replaced by
+    their rotated queries. V rows are copied unchanged.
+    """
+    S_max = np.asarray(k_cache).shape[2]
+    k_rot = _rope_new_rows(k_new, cos, sin, seq_lens, S_max)
+    kc, vc, lens, status = append(np.asarray(k_cache).view(np.uint16),
+                                  np.asarray(v_cache).view(np.uint16), seq_lens, k_rot,
+                                  np.asarray(v_new).view(np.uint16))
+    q_res = None
+    if q is not None:
+        q_res = _merge_rotated_queries(q, q_out, cos, sin, seq_lens, S_max)
+    return kc, vc, lens, status, q_res
+
+
+def append_paged_rope(k_pool, v_pool, block_table, seq_lens, k_new, v_new, page_size: int,
+                      cos, sin, q=None, q_out=None):
+    """``append_rope`` into a paged cache (positions are logical rows)."""
+    cap = np.asarray(block_table).shape[1] * page_size
+    k_rot = _rope_new_rows(k_new, cos, sin, seq_lens, cap)
+    kp, vp, lens, status = append_paged(np.asarray(k_pool).view(np.uint16),
+                                        np.asarray(v_pool).view(np.uint16), block_table,
+                                        seq_lens, k_rot, np.asarray(v_new).view(np.uint16),
+                                        page_size)
+    q_res = None
+    if q is not None:
+        q_res = _merge_rotated_queries(q, q_out, cos, sin, seq_lens, cap)
+    return kp, vp, lens, status, q_res
+
+
+def _merge_rotated_queries(q, q_out, cos, sin, seq_lens, capacity):
+    q_bits = np.asarray(q).view(np.uint16)
+    res = (q_bits if q_out is None else np.asarray(q_out).view(np.uint16)).copy()
+    rot = _rope_new_rows(q_bits, cos, sin, seq_lens, capacity)
+    B, T = q_bits.shape[:2]
+    for b in range(B):
+        for t in range(T):
+            if int(seq_lens[b]) + t < capacity:
+                res[b, t] = rot[b, t]
+    return res
