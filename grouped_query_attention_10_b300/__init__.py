@@ -14,5 +14,7 @@ from .binding import (  # noqa: F401
     gqa_prefill_kvcache_fwd,
     gqa_status_string,
     kv_cache_append,
+    kv_cache_append_paged_rope,
+    kv_cache_append_rope,
     load_library,
 )

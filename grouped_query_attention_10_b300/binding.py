@@ -76,6 +76,12 @@ def load_library() -> ctypes.CDLL:
     lib.kv_cache_append_paged.argtypes = [vp, vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, i32,
                                           i32, vp, vp]
     lib.kv_cache_append_paged.restype = i32
+    lib.kv_cache_append_rope.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i32, i32, i32, i32,
+                                         i32, i32, i32, vp, vp]
+    lib.kv_cache_append_rope.restype = i32
+    lib.kv_cache_append_paged_rope.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, i32, i32,
+                                               i32, i32, i32, i32, i32, i32, i32, vp, vp]
+    lib.kv_cache_append_paged_rope.restype = i32
     lib.gqa_decode_workspace_bytes.argtypes = [i32, i32, i32, i32, i32]
     lib.gqa_decode_workspace_bytes.restype = sz
     lib.gqa_decode_fwd.argtypes = [vp, vp, vp, vp, vp, i32, vp, i32, i32, i32, i32, i32, f32,
@@ -382,3 +388,78 @@ def kv_cache_append_paged(k_pool: torch.Tensor, v_pool: torch.Tensor,
                                    _stream_ptr(stream, k_pool.device))
     if rc != GQA_OK:
         raise GQAError(rc, "kv_cache_append_paged")
+
+
+def _rope_operands(q, q_out, rope_cos, rope_sin, B, T, d):
+    _check(rope_cos, "rope_cos", torch.float32)
+    n_pos = rope_cos.shape[0]
+    _check(rope_cos, "rope_cos", torch.float32, (n_pos, d // 2))
+    _check(rope_sin, "rope_sin", torch.float32, (n_pos, d // 2))
+    h_q = 0
+    if q is not None:
+        h_q = q.shape[2]
+        _check(q, "q", torch.bfloat16, (B, T, h_q, d))
+        if q_out is None:
+            q_out = q
+        _check(q_out, "q_out", torch.bfloat16, (B, T, h_q, d))
+    elif q_out is not None:
+        raise ValueError("q_out given without q")
+    return q_out, n_pos, h_q
+
+
+def kv_cache_append_rope(k_cache: torch.Tensor, v_cache: torch.Tensor, seq_lens: torch.Tensor,
+                         k_new: torch.Tensor, v_new: torch.Tensor, rope_cos: torch.Tensor,
+                         rope_sin: torch.Tensor, *, q: Optional[torch.Tensor] = None,
+                         q_out: Optional[torch.Tensor] = None,
+                         status: Optional[torch.Tensor] = None, stream=None):
+    """kv_cache_append with RoPE: keys rotated into the cache at their rows,
+    values copied, and (if q is given) the same tokens' queries rotated into
+    q_out (default: in place). Returns q_out (or None)."""
+    lib = load_library()
+    B, g, S_max, d = k_cache.shape
+    T = k_new.shape[1]
+    _check(k_cache, "k_cache", torch.bfloat16)
+    _check(v_cache, "v_cache", torch.bfloat16, (B, g, S_max, d))
+    _check(seq_lens, "seq_lens", torch.int32, (B,))
+    _check(k_new, "k_new", torch.bfloat16, (B, T, g, d))
+    _check(v_new, "v_new", torch.bfloat16, (B, T, g, d))
+    q_out, n_pos, h_q = _rope_operands(q, q_out, rope_cos, rope_sin, B, T, d)
+    if status is not None:
+        _check(status, "status", torch.int32)
+    rc = lib.kv_cache_append_rope(_ptr(k_cache), _ptr(v_cache), _ptr(seq_lens), _ptr(k_new),
+                                  _ptr(v_new), _ptr(q), _ptr(q_out), _ptr(rope_cos),
+                                  _ptr(rope_sin), n_pos, B, h_q, g, d, S_max, T, _ptr(status),
+                                  _stream_ptr(stream, k_cache.device))
+    if rc != GQA_OK:
+        raise GQAError(rc, "kv_cache_append_rope")
+    return q_out
+
+
+def kv_cache_append_paged_rope(k_pool: torch.Tensor, v_pool: torch.Tensor,
+                               block_table: torch.Tensor, seq_lens: torch.Tensor,
+                               k_new: torch.Tensor, v_new: torch.Tensor, rope_cos: torch.Tensor,
+                               rope_sin: torch.Tensor, *, q: Optional[torch.Tensor] = None,
+                               q_out: Optional[torch.Tensor] = None,
+                               status: Optional[torch.Tensor] = None, stream=None):
+    """kv_cache_append_rope into a paged pool through the block table."""
+    lib = load_library()
+    num_pages, g, page_size, d = k_pool.shape
+    B, max_blocks = block_table.shape
+    T = k_new.shape[1]
+    _check(k_pool, "k_pool", torch.bfloat16)
+    _check(v_pool, "v_pool", torch.bfloat16, (num_pages, g, page_size, d))
+    _check(block_table, "block_table", torch.int32, (B, max_blocks))
+    _check(seq_lens, "seq_lens", torch.int32, (B,))
+    _check(k_new, "k_new", torch.bfloat16, (B, T, g, d))
+    _check(v_new, "v_new", torch.bfloat16, (B, T, g, d))
+    q_out, n_pos, h_q = _rope_operands(q, q_out, rope_cos, rope_sin, B, T, d)
+    if status is not None:
+        _check(status, "status", torch.int32)
+    rc = lib.kv_cache_append_paged_rope(_ptr(k_pool), _ptr(v_pool), _ptr(block_table),
+                                        _ptr(seq_lens), _ptr(k_new), _ptr(v_new), _ptr(q),
+                                        _ptr(q_out), _ptr(rope_cos), _ptr(rope_sin), n_pos, B,
+                                        h_q, g, d, page_size, num_pages, max_blocks, T,
+                                        _ptr(status), _stream_ptr(stream, k_pool.device))
+    if rc != GQA_OK:
+        raise GQAError(rc, "kv_cache_append_paged_rope")
+    return q_out

@@ -407,6 +407,121 @@ int kv_cache_append_paged(void* k_pool, void* v_pool, const int32_t* block_table
              : GQA_ERR_CUDA;
 }
 
+}  // extern "C"
+
+namespace {
+
+// Checks shared by the two RoPE appends; `cap` is the logical capacity.
+int rope_append_check(const void* k_new, const void* v_new, const void* q, void* q_out,
+                      const float* rope_cos, const float* rope_sin, int rope_n_pos, int B,
+                      int h_q, int g, int d, int T, long long cap) {
+  if (k_new == nullptr || v_new == nullptr || rope_cos == nullptr || rope_sin == nullptr)
+    return GQA_ERR_NULL;
+  if ((q == nullptr) != (q_out == nullptr)) return GQA_ERR_NULL;
+  if (B < 1 || g < 1 || (d != 64 && d != 128) || T < 0) return GQA_ERR_SHAPE;
+  if (q != nullptr && !heads_ok(h_q, g, d)) return GQA_ERR_SHAPE;
+  // every stored row's position must have a table row
+  if (rope_n_pos < cap || static_cast<long long>(rope_n_pos) * d >= kMaxElems)
+    return GQA_ERR_SHAPE;
+  const long long qn = q != nullptr ? static_cast<long long>(B) * T * h_q * d : 0;
+  if (static_cast<long long>(B) * T * g * d >= kMaxElems || qn >= kMaxElems) return GQA_ERR_SHAPE;
+  if (q != nullptr && q != q_out) {
+    // the rotated queries go in place or to a buffer that does not overlap q
+    const uintptr_t a0 = reinterpret_cast<uintptr_t>(q), b0 = reinterpret_cast<uintptr_t>(q_out);
+    const uintptr_t n = static_cast<uintptr_t>(qn) * 2;
+    if (a0 < b0 + n && b0 < a0 + n) return GQA_ERR_SHAPE;
+  }
+  if (!aligned16(k_new) || !aligned16(v_new) || !aligned16(rope_cos) || !aligned16(rope_sin))
+    return GQA_ERR_ALIGN;
+  if (q != nullptr && (!aligned16(q) || !aligned16(q_out))) return GQA_ERR_ALIGN;
+  return GQA_OK;
+}
+
+int rope_append_launch(gqa::RopeAppendArgs& a, void* stream) {
+  if (a.T == 0) return GQA_OK;
+  return gqa::launch_append_rope(a, static_cast<cudaStream_t>(stream)) == cudaSuccess
+             ? GQA_OK
+             : GQA_ERR_CUDA;
+}
+
+}  // namespace
+
+extern "C" {
+
+int kv_cache_append_rope(void* k_cache, void* v_cache, int32_t* seq_lens, const void* k_new,
+                         const void* v_new, const void* q, void* q_out, const float* rope_cos,
+                         const float* rope_sin, int rope_n_pos, int B, int h_q, int g, int d,
+                         int S_max, int T, int32_t* status_dev, void* stream) {
+  if (k_cache == nullptr || v_cache == nullptr || seq_lens == nullptr) return GQA_ERR_NULL;
+  if (S_max < 1) return GQA_ERR_SHAPE;
+  int rc = rope_append_check(k_new, v_new, q, q_out, rope_cos, rope_sin, rope_n_pos, B, h_q, g,
+                             d, T, S_max);
+  if (rc != GQA_OK) return rc;
+  if (static_cast<long long>(B) * g * S_max * d >= kMaxElems) return GQA_ERR_SHAPE;
+  if (!aligned16(k_cache) || !aligned16(v_cache) || !aligned4(seq_lens)) return GQA_ERR_ALIGN;
+  if (status_dev != nullptr && !aligned4(status_dev)) return GQA_ERR_ALIGN;
+  gqa::RopeAppendArgs a{};
+  a.k_dst = k_cache;
+  a.v_dst = v_cache;
+  a.table = nullptr;
+  a.S_max = S_max;
+  a.seq_lens = seq_lens;
+  a.k_new = k_new;
+  a.v_new = v_new;
+  a.q = q;
+  a.q_out = q_out;
+  a.cos = rope_cos;
+  a.sin = rope_sin;
+  a.B = B;
+  a.T = T;
+  a.h_q = q != nullptr ? h_q : 0;
+  a.g = g;
+  a.d = d;
+  a.status = status_dev;
+  return rope_append_launch(a, stream);
+}
+
+int kv_cache_append_paged_rope(void* k_pool, void* v_pool, const int32_t* block_table,
+                               int32_t* seq_lens, const void* k_new, const void* v_new,
+                               const void* q, void* q_out, const float* rope_cos,
+                               const float* rope_sin, int rope_n_pos, int B, int h_q, int g,
+                               int d, int page_size, int num_pages, int max_blocks, int T,
+                               int32_t* status_dev, void* stream) {
+  if (k_pool == nullptr || v_pool == nullptr || block_table == nullptr || seq_lens == nullptr)
+    return GQA_ERR_NULL;
+  if (num_pages < 1 || !paged_ok(page_size, max_blocks)) return GQA_ERR_SHAPE;
+  int rc = rope_append_check(k_new, v_new, q, q_out, rope_cos, rope_sin, rope_n_pos, B, h_q, g,
+                             d, T, static_cast<long long>(page_size) * max_blocks);
+  if (rc != GQA_OK) return rc;
+  if (static_cast<long long>(num_pages) * g * page_size * d >= kMaxElems ||
+      static_cast<long long>(B) * max_blocks >= (1LL << 31))
+    return GQA_ERR_SHAPE;
+  if (!aligned16(k_pool) || !aligned16(v_pool) || !aligned4(seq_lens) || !aligned4(block_table))
+    return GQA_ERR_ALIGN;
+  if (status_dev != nullptr && !aligned4(status_dev)) return GQA_ERR_ALIGN;
+  gqa::RopeAppendArgs a{};
+  a.k_dst = k_pool;
+  a.v_dst = v_pool;
+  a.table = block_table;
+  a.page_log2 = log2i(page_size);
+  a.num_pages = num_pages;
+  a.max_blocks = max_blocks;
+  a.seq_lens = seq_lens;
+  a.k_new = k_new;
+  a.v_new = v_new;
+  a.q = q;
+  a.q_out = q_out;
+  a.cos = rope_cos;
+  a.sin = rope_sin;
+  a.B = B;
+  a.T = T;
+  a.h_q = q != nullptr ? h_q : 0;
+  a.g = g;
+  a.d = d;
+  a.status = status_dev;
+  return rope_append_launch(a, stream);
+}
+
 int kv_cache_append(void* k_cache, void* v_cache, int32_t* seq_lens, const void* k_new,
                     const void* v_new, int B, int g, int d, int S_max, int T,
                     int32_t* status_dev, void* stream) {

@@ -114,6 +114,154 @@ cudaError_t launch_append_paged(void* k_pool, void* v_pool, const int32_t* block
   return cudaGetLastError();
 }
 
+// ---------------------------------------------------------------------------
+// RoPE append: one launch rotates the new tokens' query rows (into q_out) and
+// key rows (into the cache) and copies their value rows, at the position each
+// token takes in the cache (seq_lens[b] + t). The rotation is the RoPE code of
+// the jsqmd.com attention survey, chapter 1: pair (x[2i], x[2i+1]) is turned
+// by the angle of table row `pos`, the turned even parts fill the first half
+// of the output row and the turned odd parts the second half. Arithmetic is
+// binary32 with every product, sum and difference rounded (no contraction),
+// as the survey's code evaluates bf16 rows times fp32 tables; the stored
+// value is rounded to bf16.
+//
+// One thread per (row, u): input chunks 2u and 2u+1 (16 elements = 8 pairs)
+// give output chunks u and u + d/16 of a rotated row; a value row is copied
+// as chunks 2u and 2u+1. The loop is uniform per warp and every lane reads
+// before any lane writes (a row never spans two warps), so q_out may be q.
+// One pair: w holds input elements 2i (low half) and 2i+1 (high half).
+__device__ __forceinline__ void rope_pair(uint32_t w, float c, float s, float* first,
+                                          float* second) {
+  const float e = __uint_as_float(w << 16);
+  const float o = __uint_as_float(w & 0xffff0000u);
+  *first = __fsub_rn(__fmul_rn(e, c), __fmul_rn(o, s));
+  *second = __fadd_rn(__fmul_rn(e, s), __fmul_rn(o, c));
+}
+
+__device__ __forceinline__ uint32_t pack_bf16_rn(float lo, float hi) {
+  const __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<const uint32_t*>(&v);
+}
+
+template <bool PAGED>
+__global__ void __launch_bounds__(256) kv_append_rope_kernel(const RopeAppendArgs a) {
+  const int half = a.d / 16;   // threads per row
+  const int chunks = a.d / 8;  // 16-byte chunks per row
+  const int rows_bt = a.h_q + 2 * a.g;  // query, key and value rows of one token
+  const long long total = static_cast<long long>(a.B) * a.T * rows_bt * half;
+  const int cap = PAGED ? (a.max_blocks << a.page_log2) : a.S_max;
+  const int lane = threadIdx.x & 31;
+  const long long stride = static_cast<long long>(gridDim.x) * blockDim.x;
+  const float4* cos4 = reinterpret_cast<const float4*>(a.cos);
+  const float4* sin4 = reinterpret_cast<const float4*>(a.sin);
+  for (long long base = static_cast<long long>(blockIdx.x) * blockDim.x + (threadIdx.x & ~31);
+       base < total; base += stride) {
+    const long long idx = base + lane;
+    bool act = idx < total;
+    uint4 out0 = make_uint4(0u, 0u, 0u, 0u), out1 = out0;
+    uint4* dst0 = nullptr;
+    uint4* dst1 = nullptr;
+    if (act) {
+      const int u = static_cast<int>(idx % half);
+      const long long r = idx / half;
+      const int row = static_cast<int>(r % rows_bt);
+      const long long bt = r / rows_bt;
+      const int t = static_cast<int>(bt % a.T);
+      const int b = static_cast<int>(bt / a.T);
+      const int len = a.seq_lens[b];
+      int pos = 0;
+      if (len < 0 || len > cap) {
+        if (t == 0 && row == 0 && u == 0) record_status(a.status, GQA_ERR_BAD_LENGTH);
+        act = false;
+      } else {
+        pos = len + t;
+        if (pos >= cap) {
+          if (row == 0 && u == 0) record_status(a.status, GQA_ERR_CACHE_FULL);
+          act = false;
+        }
+      }
+      const uint4* src = nullptr;
+      uint4* drow = nullptr;
+      bool rotate = true;
+      if (act) {
+        if (row < a.h_q) {
+          const size_t off = (static_cast<size_t>(bt) * a.h_q + row) * chunks;
+          src = static_cast<const uint4*>(a.q) + off;
+          drow = static_cast<uint4*>(a.q_out) + off;
+        } else {
+          int h = row - a.h_q;
+          const bool value = h >= a.g;
+          if (value) h -= a.g;
+          rotate = !value;
+          src = static_cast<const uint4*>(value ? a.v_new : a.k_new) +
+                (static_cast<size_t>(bt) * a.g + h) * chunks;
+          size_t dst_row;
+          if (PAGED) {
+            const int page = a.table[static_cast<size_t>(b) * a.max_blocks + (pos >> a.page_log2)];
+            if (page < 0 || page >= a.num_pages) {
+              if (u == 0) record_status(a.status, GQA_ERR_BAD_PAGE);
+              act = false;
+            }
+            dst_row = (static_cast<size_t>(page) * a.g + h) << a.page_log2 |
+                      static_cast<size_t>(pos & ((1 << a.page_log2) - 1));
+          } else {
+            dst_row = (static_cast<size_t>(b) * a.g + h) * a.S_max + static_cast<size_t>(pos);
+          }
+          drow = static_cast<uint4*>(value ? a.v_dst : a.k_dst) + dst_row * chunks;
+        }
+      }
+      if (act) {
+        const uint4 x0 = src[2 * u];
+        const uint4 x1 = src[2 * u + 1];
+        if (rotate) {
+          const size_t trow = static_cast<size_t>(pos) * (a.d / 8);  // float4s per table row
+          const float4 c0 = cos4[trow + 2 * u], c1 = cos4[trow + 2 * u + 1];
+          const float4 s0 = sin4[trow + 2 * u], s1 = sin4[trow + 2 * u + 1];
+          const uint32_t w[8] = {x0.x, x0.y, x0.z, x0.w, x1.x, x1.y, x1.z, x1.w};
+          const float cv[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
+          const float sv[8] = {s0.x, s0.y, s0.z, s0.w, s1.x, s1.y, s1.z, s1.w};
+          float f[8], g2[8];
+#pragma unroll
+          for (int j = 0; j < 8; ++j) rope_pair(w[j], cv[j], sv[j], &f[j], &g2[j]);
+          out0 = make_uint4(pack_bf16_rn(f[0], f[1]), pack_bf16_rn(f[2], f[3]),
+                            pack_bf16_rn(f[4], f[5]), pack_bf16_rn(f[6], f[7]));
+          out1 = make_uint4(pack_bf16_rn(g2[0], g2[1]), pack_bf16_rn(g2[2], g2[3]),
+                            pack_bf16_rn(g2[4], g2[5]), pack_bf16_rn(g2[6], g2[7]));
+          dst0 = drow + u;
+          dst1 = drow + u + half;
+        } else {
+          out0 = x0;
+          out1 = x1;
+          dst0 = drow + 2 * u;
+          dst1 = drow + 2 * u + 1;
+        }
+      }
+    }
+    __syncwarp();  // every lane has read its row chunks (q_out may alias q)
+    if (act) {
+      *dst0 = out0;
+      *dst1 = out1;
+    }
+  }
+}
+
+cudaError_t launch_append_rope(const RopeAppendArgs& a, cudaStream_t s) {
+  const long long total = static_cast<long long>(a.B) * a.T * (a.h_q + 2 * a.g) * (a.d / 16);
+  long long blocks = (total + 255) / 256;
+  if (blocks > 148LL * 16) blocks = 148LL * 16;  // grid-stride beyond 16 CTAs per SM
+  if (blocks < 1) blocks = 1;
+  const bool paged = a.table != nullptr;
+  if (paged)
+    kv_append_rope_kernel<true><<<static_cast<unsigned>(blocks), 256, 0, s>>>(a);
+  else
+    kv_append_rope_kernel<false><<<static_cast<unsigned>(blocks), 256, 0, s>>>(a);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  const int cap = paged ? (a.max_blocks << a.page_log2) : a.S_max;
+  kv_append_lens_kernel<<<(a.B + 127) / 128, 128, 0, s>>>(a.seq_lens, a.B, cap, a.T);
+  return cudaGetLastError();
+}
+
 cudaError_t launch_append(void* k_cache, void* v_cache, int32_t* seq_lens, const void* k_new,
                           const void* v_new, int B, int g, int d, int S_max, int T,
                           int32_t* status, cudaStream_t s) {

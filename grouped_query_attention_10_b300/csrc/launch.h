@@ -68,4 +68,23 @@ cudaError_t launch_append_paged(void* k_pool, void* v_pool, const int32_t* block
 // Split length (tokens per split-KV CTA) used for these decode sizes.
 int decode_split_len(int B, int h_q, int g, int S_max);
 
+// RoPE append (contiguous cache when table == nullptr, else paged pool).
+struct RopeAppendArgs {
+  void* k_dst;                // [B, g, S_max, d] cache or [num_pages, g, page_size, d] pool
+  void* v_dst;
+  const int32_t* table;       // [B, max_blocks] page ids, or nullptr
+  int page_log2, num_pages, max_blocks;
+  int S_max;
+  int32_t* seq_lens;
+  const void* k_new;          // [B, T, g, d]
+  const void* v_new;
+  const void* q;              // [B, T, h_q, d] or nullptr (then h_q = 0)
+  void* q_out;
+  const float* cos;           // [n_pos, d / 2]
+  const float* sin;
+  int B, T, h_q, g, d;
+  int32_t* status;
+};
+cudaError_t launch_append_rope(const RopeAppendArgs& a, cudaStream_t s);
+
 }  // namespace gqa

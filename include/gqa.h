@@ -246,6 +246,51 @@ int kv_cache_append_paged(void* k_pool, void* v_pool, const int32_t* block_table
                           int32_t* status_dev, void* stream);
 
 /*
+ * kv_cache_append_rope -- kv_cache_append with the rotary position embedding
+ * of the jsqmd.com attention survey (chapter 1, RoPE code; chapter 5 names
+ * the fused-RoPE build option) applied on the way in, in one launch (plus
+ * the length update):
+ *   - key rows are rotated before they are stored, value rows are copied;
+ *   - if q is given, the same tokens' query rows are rotated into q_out.
+ * Token t of sequence b takes position p = seq_lens[b] + t (its cache row).
+ * For each row x (d elements) and i < d/2:
+ *     out[i]       = x[2i] * cos[p][i] - x[2i+1] * sin[p][i]
+ *     out[d/2 + i] = x[2i] * sin[p][i] + x[2i+1] * cos[p][i]
+ * evaluated in binary32 with each product, sum and difference rounded (no
+ * fused multiply-add), then rounded to bf16 (nearest, ties to even).
+ *
+ *   k_cache, v_cache, seq_lens, k_new, v_new, B, g, d, S_max, T
+ *                   as in kv_cache_append (k_new/v_new must not overlap the cache)
+ *   q, q_out        device bf16 [B, T, h_q, d], both NULL or both given;
+ *                   q_out == q rotates in place, otherwise the two must not
+ *                   overlap. Query rows of tokens dropped for lack of room
+ *                   are not written. h_q is ignored when q is NULL.
+ *   rope_cos, rope_sin
+ *                   device fp32 [rope_n_pos, d/2], row p = the cosines and
+ *                   sines of position p; 16-byte aligned; rope_n_pos must be
+ *                   >= S_max (every cache row has a table row)
+ *
+ * Errors as in kv_cache_append (GQA_ERR_CACHE_FULL / GQA_ERR_BAD_LENGTH in
+ * *status_dev); sizes out of range are GQA_ERR_SHAPE.
+ */
+int kv_cache_append_rope(void* k_cache, void* v_cache, int32_t* seq_lens, const void* k_new,
+                         const void* v_new, const void* q, void* q_out, const float* rope_cos,
+                         const float* rope_sin, int rope_n_pos, int B, int h_q, int g, int d,
+                         int S_max, int T, int32_t* status_dev, void* stream);
+
+/*
+ * kv_cache_append_paged_rope -- kv_cache_append_rope into a paged cache
+ * (positions are logical rows; rope_n_pos >= page_size * max_blocks). A
+ * block-table entry outside the pool for a stored row is GQA_ERR_BAD_PAGE.
+ */
+int kv_cache_append_paged_rope(void* k_pool, void* v_pool, const int32_t* block_table,
+                               int32_t* seq_lens, const void* k_new, const void* v_new,
+                               const void* q, void* q_out, const float* rope_cos,
+                               const float* rope_sin, int rope_n_pos, int B, int h_q, int g,
+                               int d, int page_size, int num_pages, int max_blocks, int T,
+                               int32_t* status_dev, void* stream);
+
+/*
  * gqa_decode_fwd_noalloc -- gqa_decode_fwd for callers that cannot allocate.
  * The pages have no counterpart of this entry point; it exists for callers
  * that cannot hand over a workspace: plugin hosts that pass a library only

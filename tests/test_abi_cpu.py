@@ -178,3 +178,30 @@ def test_paged_entry_points_validation(lib):
     assert app(table=None) == binding.GQA_ERR_NULL
     assert app(page=100) == binding.GQA_ERR_SHAPE
     assert app(T=0) == binding.GQA_OK
+
+
+def test_rope_append_validation(lib):
+    f = FAKE
+
+    def app(q=f, q_out=f, cos=f, n_pos=4096, h_q=32, g=8, d=128, S=4096, T=1):
+        # k_cache, v_cache, seq_lens, k_new, v_new, q, q_out, cos, sin, n_pos, B, h_q, g, d,
+        # S_max, T, status, stream
+        return lib.kv_cache_append_rope(f, f, f, f, f, q, q_out, cos, f, n_pos, 2, h_q, g, d, S,
+                                        T, None, None)
+    assert app(cos=None) == binding.GQA_ERR_NULL
+    assert app(q_out=None) == binding.GQA_ERR_NULL          # q without q_out
+    assert app(n_pos=4095) == binding.GQA_ERR_SHAPE          # a cache row without a table row
+    assert app(h_q=12) == binding.GQA_ERR_SHAPE              # group size not a power of two
+    assert app(d=96) == binding.GQA_ERR_SHAPE
+    assert app(q_out=FAKE + 64) == binding.GQA_ERR_SHAPE     # q_out overlaps q partly
+    assert app(cos=FAKE + 4) == binding.GQA_ERR_ALIGN
+    assert app(T=0) == binding.GQA_OK                        # nothing to do, nothing queued
+    assert app(q=None, q_out=None, T=0) == binding.GQA_OK
+
+    def papp(table=f, page=64, blocks=16, n_pos=1024, T=1):
+        return lib.kv_cache_append_paged_rope(f, f, table, f, f, f, f, f, f, f, n_pos, 2, 32, 8,
+                                              128, page, 100, blocks, T, None, None)
+    assert papp(table=None) == binding.GQA_ERR_NULL
+    assert papp(page=48) == binding.GQA_ERR_SHAPE
+    assert papp(n_pos=1023) == binding.GQA_ERR_SHAPE          # capacity 64 * 16 = 1024
+    assert papp(T=0) == binding.GQA_OK
