@@ -282,23 +282,64 @@ def native_arm(args):
     flops_step = flops_prefill + accounting.decode_flops([S_max] * B, h_q, d)
     launches_per_step = 2 + 1 + 2 + 2  # append(rows, lens), prefill, append, decode(split, combine)
 
-    def step(ev_p0=None, ev_p1=None):
-        lens.zero_()
-        gqa.kv_cache_append(kc, vc, lens, k, v, status=status, stream=stream)
-        if ev_p0 is not None:
-            ev_p0.record(stream)
-        gqa.gqa_prefill_fwd(q, k, v, causal=w.causal, scale=w.scale, out=o, status=status,
-                            stream=stream)
-        if ev_p1 is not None:
-            ev_p1.record(stream)
-        gqa.kv_cache_append(kc, vc, lens, k_new, v_new, status=status, stream=stream)
-        gqa.gqa_decode_fwd(q_new, kc, vc, lens, scale=w.scale, out=od, workspace=ws,
-                           status=status, stream=stream)
+    def step_parts(s):
+        # the step in three parts, split where the prefill is timed on its own
+        def pre():
+            lens.zero_()
+            gqa.kv_cache_append(kc, vc, lens, k, v, status=status, stream=s)
+
+        def pf():
+            gqa.gqa_prefill_fwd(q, k, v, causal=w.causal, scale=w.scale, out=o, status=status,
+                                stream=s)
+
+        def post():
+            gqa.kv_cache_append(kc, vc, lens, k_new, v_new, status=status, stream=s)
+            gqa.gqa_decode_fwd(q_new, kc, vc, lens, scale=w.scale, out=od, workspace=ws,
+                               status=status, stream=s)
+        return pre, pf, post
+
+    eager_parts = step_parts(stream)
+
+    def step():
+        for fn in eager_parts:
+            fn()
 
     for _ in range(max(args.warmup, 3)):
         flush()
         step()
     torch.cuda.synchronize()
+    o_eager, od_eager = o.clone(), od.clone()
+
+    # The timed steps replay the same library calls captured as CUDA graphs
+    # (the launches of the small append / decode kernels then follow each
+    # other without host round trips); the results must equal the eager ones.
+    cap = torch.cuda.Stream(dev)
+    cap.wait_stream(stream)
+    graphs = []
+    with torch.cuda.stream(cap):
+        for fn in step_parts(cap):
+            gr = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(gr, stream=cap):
+                fn()
+            graphs.append(gr)
+    torch.cuda.synchronize()
+    g_pre, g_pf, g_post = graphs
+
+    def step_graph(ev_p0=None, ev_p1=None):
+        g_pre.replay()
+        if ev_p0 is not None:
+            ev_p0.record(stream)
+        g_pf.replay()
+        if ev_p1 is not None:
+            ev_p1.record(stream)
+        g_post.replay()
+
+    for _ in range(3):
+        flush()
+        step_graph()
+    torch.cuda.synchronize()
+    if not (torch.equal(o, o_eager) and torch.equal(od, od_eager)):
+        raise RuntimeError("graph replay of the step differs from the eager calls")
 
     evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
     barrier()
@@ -308,7 +349,7 @@ def native_arm(args):
             flush()  # L2 flush between timed steps, outside the timed interval
             e0, ep0, ep1, e1 = evs[i]
             e0.record(stream)
-            step(ep0, ep1)
+            step_graph(ep0, ep1)
             e1.record(stream)
         torch.cuda.synchronize()
     barrier()
@@ -387,6 +428,8 @@ def native_arm(args):
                    "B": B, "L": L, "h_q": h_q, "g": g, "d": d, "causal": False,
                    "step": "append prompt K/V, prefill, append 1 token, decode 1 token",
                    "l2": "flushed between timed steps (256 MiB write, then 256 MiB read)",
+                   "launch": "each step replays three CUDA graphs of the library calls "
+                             "(reset + prompt append | prefill | token append + decode)",
                    "parallelism": f"replicas x{world}"},
         "roofline": roofline,
         "e2e": e2e,
