@@ -554,33 +554,26 @@ __global__ void __launch_bounds__(kCombineThreads) decode_combine_kernel(
 }
 
 int decode_split_len(int B, int h_q, int g, int S_max) {
-  // Pick the split length (a multiple of the 64-token stage) that minimises
-  // the modelled time of the split pass when every sequence is full: the
-  // persistent CTAs (two per SM of a 148-SM B300) fetch items one by one, so
-  // the slowest CTA handles about ceil(items / CTAs) items of split_len
-  // tokens each, plus a fixed cost per item (query load, partial write) worth
-  // about two stages. With fewer than two items per CTA nothing can even out
-  // CTAs that stream slower than others, so such a choice pays one more item
-  // length. Only performance depends on this choice.
+  // The split pass streams the cache from HBM, which all CTAs share: once
+  // enough CTAs are streaming, the total time is the cache bytes over the
+  // bandwidth plus per-item costs (query load, partial write, and the
+  // combine's reads of the partials), so fewer, longer items are better as
+  // long as every CTA slot (two per SM of a 148-SM B300) gets one. Choose the
+  // fewest splits per segment that give at least 80 % of the slots an item,
+  // and cap an item at 2048 tokens so that sequences of very different
+  // lengths still even out over the dynamic fetch. Only performance depends
+  // on this choice.
   constexpr long long kSlots = 148LL * kCtasPerSm;
-  constexpr long long kItemCost = 2 * kDecodeStage;
+  constexpr long long kMaxLen = 2048;
   const long long G = h_q / g;
-  const long long pairs = static_cast<long long>(B) * g * ((G + 31) / 32);
-  const long long s_cap = (static_cast<long long>(S_max) + kDecodeStage - 1) / kDecodeStage *
-                          kDecodeStage;
-  long long best_len = s_cap, best_cost = -1;
-  for (long long len = kDecodeStage; len <= 4096 && len < s_cap + kDecodeStage;
-       len += kDecodeStage) {
-    const long long l = len < s_cap ? len : s_cap;
-    const long long items = pairs * ((S_max + l - 1) / l);
-    const long long waves = (items + kSlots - 1) / kSlots;
-    const long long cost = waves * (l + kItemCost) + (items < 2 * kSlots ? l : 0);
-    if (best_cost < 0 || cost < best_cost) {
-      best_cost = cost;
-      best_len = l;
-    }
-  }
-  return static_cast<int>(best_len);
+  const long long segs = static_cast<long long>(B) * g * ((G + 31) / 32);
+  const long long want = (kSlots * 4 + 4) / 5;  // 80 % of the slots
+  const long long n_split = segs >= want ? 1 : (want + segs - 1) / segs;
+  long long l = (static_cast<long long>(S_max) + n_split - 1) / n_split;
+  l = (l + kDecodeStage - 1) / kDecodeStage * kDecodeStage;
+  if (l > kMaxLen) l = kMaxLen;
+  if (l < kDecodeStage) l = kDecodeStage;
+  return static_cast<int>(l);
 }
 
 namespace {
