@@ -305,7 +305,7 @@ int kv_cache_append_paged_rope(void* k_pool, void* v_pool, const int32_t* block_
  * nothing. Sizes whose gqa_decode_workspace_bytes exceeds the array are
  * rejected with GQA_ERR_SCRATCH_LIMIT before anything is queued (for
  * d = 128, h_q = 32, g = 8 the ragged B = 64, S_max = 8192 cache needs about
- * 17 MiB).
+ * 16 MiB).
  *
  *  - The first call made while a device is current looks up the array's
  *    device address on that device (cudaGetSymbolAddress) and keeps it; make
