@@ -354,3 +354,29 @@ def test_append_full_size_decode_workload():
     for b in range(1, w.B):
         mask[b, :, int(lb[b])] = False
     assert torch.equal(kc[mask].view(torch.int16), k_before[mask].view(torch.int16))
+
+
+@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("h_q,g", [(16, 1), (64, 2), (128, 1), (32, 2)])
+def test_decode_large_groups_tensor_core_path(d, h_q, g):
+    """Groups of 16..128 query heads (the tcgen05 consumer): ragged lengths
+    including 0, 1 and stage boundaries, garbage past the lengths."""
+    B, S = 6, 4500
+    q = rand_bf16((B, h_q, d), 81 + h_q)
+    kc = rand_bf16((B, g, S, d), 82 + h_q)
+    vc = rand_bf16((B, g, S, d), 83 + h_q)
+    lens_l = [4500, 0, 1, 63, 65, 2049]
+    lens = torch.tensor(lens_l, dtype=torch.int32, device=DEV)
+    o_clean, lse_clean = run_decode(q, kc, vc, lens, 1.0 / math.sqrt(d))
+    for b, n in enumerate(lens_l):
+        kc[b, :, n:] = float("nan")
+        vc[b, :, n:] = float("inf")
+    o, lse = run_decode(q, kc, vc, lens, 1.0 / math.sqrt(d))
+    assert torch.equal(o, o_clean) and torch.equal(lse, lse_clean)
+    assert torch.all(o[1] == 0) and torch.all(torch.isneginf(lse[1]))
+    o_ref, lse_ref = oracle.decode(f64(q), f64(kc), f64(vc), lens_l, 1.0 / math.sqrt(d))
+    assert_close(f64(o), o_ref, f"decode G={h_q // g} d={d}")
+    keep = [b for b, n in enumerate(lens_l) if n > 0]  # the empty row's lse is -inf (checked above)
+    assert_close(f64(lse)[keep], lse_ref[keep], f"decode lse G={h_q // g} d={d}")
+    o16, _ = run_decode(q, kc, vc, lens, 1.0 / math.sqrt(d), out_dtype=torch.bfloat16)
+    assert_close(f64(o16), o_ref, "bf16 out", max_abs=2e-2)
