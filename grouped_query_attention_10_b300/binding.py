@@ -76,6 +76,8 @@ def load_library() -> ctypes.CDLL:
     lib.kv_cache_append_paged.argtypes = [vp, vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, i32,
                                           i32, vp, vp]
     lib.kv_cache_append_paged.restype = i32
+    lib.gqa_selftest_bounded_wait.argtypes = [vp, i32, vp]
+    lib.gqa_selftest_bounded_wait.restype = i32
     lib.kv_cache_append_rope.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i32, i32, i32, i32,
                                          i32, i32, i32, vp, vp]
     lib.kv_cache_append_rope.restype = i32
@@ -463,3 +465,14 @@ def kv_cache_append_paged_rope(k_pool: torch.Tensor, v_pool: torch.Tensor,
     if rc != GQA_OK:
         raise GQAError(rc, "kv_cache_append_paged_rope")
     return q_out
+
+
+def gqa_selftest_bounded_wait(status: torch.Tensor, limit_us: int = 1000, stream=None) -> None:
+    """Run the kernels' bounded wait against a barrier that never completes;
+    ``status`` (device int32) then holds GQA_ERR_TIMEOUT."""
+    lib = load_library()
+    _check(status, "status", torch.int32)
+    rc = lib.gqa_selftest_bounded_wait(_ptr(status), int(limit_us),
+                                       _stream_ptr(stream, status.device))
+    if rc != GQA_OK:
+        raise GQAError(rc, "gqa_selftest_bounded_wait")

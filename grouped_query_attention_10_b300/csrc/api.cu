@@ -522,6 +522,16 @@ int kv_cache_append_paged_rope(void* k_pool, void* v_pool, const int32_t* block_
   return rope_append_launch(a, stream);
 }
 
+int gqa_selftest_bounded_wait(int32_t* status_dev, int limit_us, void* stream) {
+  if (status_dev == nullptr) return GQA_ERR_NULL;
+  if (limit_us < 1 || limit_us > 2000000) return GQA_ERR_SHAPE;
+  if (!aligned4(status_dev)) return GQA_ERR_ALIGN;
+  return gqa::launch_bounded_wait_selftest(status_dev, static_cast<long long>(limit_us) * 1000,
+                                           static_cast<cudaStream_t>(stream)) == cudaSuccess
+             ? GQA_OK
+             : GQA_ERR_CUDA;
+}
+
 int kv_cache_append(void* k_cache, void* v_cache, int32_t* seq_lens, const void* k_new,
                     const void* v_new, int B, int g, int d, int S_max, int T,
                     int32_t* status_dev, void* stream) {

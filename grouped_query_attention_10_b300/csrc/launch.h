@@ -87,4 +87,6 @@ struct RopeAppendArgs {
 };
 cudaError_t launch_append_rope(const RopeAppendArgs& a, cudaStream_t s);
 
+cudaError_t launch_bounded_wait_selftest(int32_t* status, long long limit_ns, cudaStream_t s);
+
 }  // namespace gqa

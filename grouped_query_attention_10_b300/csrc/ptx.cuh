@@ -75,20 +75,26 @@ __device__ __forceinline__ bool mbar_try_wait_hint(uint64_t* bar, uint32_t parit
 
 // Wait until the phase with the given parity has completed. The waiting
 // thread sleeps in hardware between polls. Gives up (and raises *abort)
-// after kWaitLimitNs, or early once another thread has raised *abort.
-// Returns false when it gave up.
-__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity,
-                                          volatile int* abort) {
+// after limit_ns (mbar_wait: kWaitLimitNs), or early once another thread has
+// raised *abort. Returns false when it gave up.
+__device__ __forceinline__ bool mbar_wait_for(uint64_t* bar, uint32_t parity, volatile int* abort,
+                                              unsigned long long limit_ns) {
   if (mbar_try_wait(bar, parity)) return true;
   const unsigned long long t0 = globaltimer_ns();
+  const uint32_t hint = limit_ns < 1000000ull ? static_cast<uint32_t>(limit_ns) : 1000000u;
   while (true) {
-    if (mbar_try_wait_hint(bar, parity, 1000000u)) return true;
+    if (mbar_try_wait_hint(bar, parity, hint)) return true;
     if (*abort) return false;
-    if (globaltimer_ns() - t0 > kWaitLimitNs) {
+    if (globaltimer_ns() - t0 > limit_ns) {
       *abort = 1;
       return false;
     }
   }
+}
+
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity,
+                                          volatile int* abort) {
+  return mbar_wait_for(bar, parity, abort, kWaitLimitNs);
 }
 
 // A short bounded wait used only while cleaning up after an abort.

@@ -291,6 +291,18 @@ int kv_cache_append_paged_rope(void* k_pool, void* v_pool, const int32_t* block_
                                int32_t* status_dev, void* stream);
 
 /*
+ * gqa_selftest_bounded_wait -- checks the failure path the kernels share,
+ * without a fault. Every wait inside the library's kernels is bounded (2 s);
+ * when one runs out the kernel stops, frees what it holds and writes
+ * GQA_ERR_TIMEOUT to its status word. This entry point launches one CTA that
+ * waits, with the same code, on a barrier nothing ever arrives at, giving up
+ * after limit_us microseconds (1 .. 2e6), so *status_dev (device int32,
+ * required) becomes GQA_ERR_TIMEOUT unless it already held an error. The
+ * device and the stream remain usable afterwards.
+ */
+int gqa_selftest_bounded_wait(int32_t* status_dev, int limit_us, void* stream);
+
+/*
  * gqa_decode_fwd_noalloc -- gqa_decode_fwd for callers that cannot allocate.
  * The pages have no counterpart of this entry point; it exists for callers
  * that cannot hand over a workspace: plugin hosts that pass a library only

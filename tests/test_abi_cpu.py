@@ -205,3 +205,10 @@ def test_rope_append_validation(lib):
     assert papp(page=48) == binding.GQA_ERR_SHAPE
     assert papp(n_pos=1023) == binding.GQA_ERR_SHAPE          # capacity 64 * 16 = 1024
     assert papp(T=0) == binding.GQA_OK
+
+
+def test_selftest_bounded_wait_validation(lib):
+    assert lib.gqa_selftest_bounded_wait(None, 1000, None) == binding.GQA_ERR_NULL
+    assert lib.gqa_selftest_bounded_wait(FAKE, 0, None) == binding.GQA_ERR_SHAPE
+    assert lib.gqa_selftest_bounded_wait(FAKE, 2000001, None) == binding.GQA_ERR_SHAPE
+    assert lib.gqa_selftest_bounded_wait(FAKE + 2, 1000, None) == binding.GQA_ERR_ALIGN
