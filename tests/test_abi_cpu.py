@@ -212,3 +212,36 @@ def test_selftest_bounded_wait_validation(lib):
     assert lib.gqa_selftest_bounded_wait(FAKE, 0, None) == binding.GQA_ERR_SHAPE
     assert lib.gqa_selftest_bounded_wait(FAKE, 2000001, None) == binding.GQA_ERR_SHAPE
     assert lib.gqa_selftest_bounded_wait(FAKE + 2, 1000, None) == binding.GQA_ERR_ALIGN
+
+
+def _expected_decode_workspace(B, h_q, g, d, S_max):
+    """The decode workspace written out from the documented rule: split
+    length = the fewest splits per segment (sequence, K/V head, 32-head slice)
+    that give 80 % of the 296 CTA slots an item, in 64-token stages, capped at
+    2048 tokens; four partials (O and log2 sum-exp) per split and query head,
+    256-byte aligned sections, then a 16-byte counter."""
+    slots, stage = 296, 64
+    segs = B * g * ((h_q // g + 31) // 32)
+    want = (slots * 4 + 4) // 5
+    n = 1 if segs >= want else -(-want // segs)
+    split = -(-S_max // n)
+    split = min(2048, max(stage, -(-split // stage) * stage))
+    n_split = -(-S_max // split)
+    rows = B * h_q * n_split * 4
+    lse_off = -(-(rows * d * 4) // 256) * 256
+    counter_off = -(-(lse_off + rows * 4) // 256) * 256
+    return counter_off + 16
+
+
+@pytest.mark.parametrize("shape", [
+    (32, 8, 4, 64, 1025),        # the bench step's decode
+    (64, 32, 8, 128, 8192),      # ragged decode workload
+    (16, 32, 1, 128, 32768),     # decode sweep g = 1
+    (16, 32, 2, 128, 32768),     # decode sweep g = 2
+    (16, 32, 32, 128, 32768),    # decode sweep g = 32
+    (1, 8, 2, 64, 129),          # smoke
+    (1, 128, 1, 64, 1),          # one row, G = 128 (four 32-head slices)
+    (300, 64, 8, 128, 100000),   # many segments: one split per 2048 tokens
+])
+def test_decode_workspace_follows_the_split_rule(lib, shape):
+    assert lib.gqa_decode_workspace_bytes(*shape) == _expected_decode_workspace(*shape)
