@@ -90,8 +90,9 @@ def test_prefill_ragged_lengths(d, causal, L):
 @pytest.mark.parametrize("h_q,g", [(4, 4), (8, 4), (8, 2), (16, 2), (32, 2), (32, 1),
                                    (64, 1), (128, 1)])
 @pytest.mark.parametrize("causal", [True, False])
-def test_prefill_group_sizes(h_q, g, causal):
-    o, lse, o_ref, lse_ref = run_prefill(1, 160, h_q, g, 64, causal, seed=7 * h_q + g)
+@pytest.mark.parametrize("d", [64, 128])
+def test_prefill_group_sizes(h_q, g, causal, d):
+    o, lse, o_ref, lse_ref = run_prefill(1, 160, h_q, g, d, causal, seed=7 * h_q + g + d)
     assert_close(f64(o), o_ref, f"prefill h_q={h_q} g={g}")
     assert_close(f64(lse), lse_ref, "lse")
 
