@@ -245,3 +245,44 @@ def _expected_decode_workspace(B, h_q, g, d, S_max):
 ])
 def test_decode_workspace_follows_the_split_rule(lib, shape):
     assert lib.gqa_decode_workspace_bytes(*shape) == _expected_decode_workspace(*shape)
+
+
+C_CLIENT = r"""
+#include <stdio.h>
+#include "gqa.h"
+int main(void) {
+  /* host-only calls: no device needed */
+  size_t ws = gqa_decode_workspace_bytes(64, 32, 8, 128, 8192);
+  int rc_null = gqa_prefill_fwd(0, 0, 0, 0, GQA_OUT_F32, 0, 1, 128, 8, 2, 64, 0.125f, 1, 0, 0);
+  int rc_shape = gqa_decode_fwd((void*)16, (void*)16, (void*)16, (const int*)16, (void*)16,
+                                GQA_OUT_F32, 0, 2, 12, 8, 128, 1024, 0.1f, (void*)16, ws, 0, 0);
+  printf("%d %zu %d %d %s\n", gqa_version(), ws, rc_null, rc_shape,
+         gqa_status_string(GQA_ERR_CACHE_FULL));
+  return 0;
+}
+"""
+
+
+def test_plain_c_client_links_and_calls_the_library(tmp_path):
+    """The boundary is a C ABI: a C99 program includes the header, links the
+    shared library and gets the documented host-side answers."""
+    import shutil
+    import subprocess
+
+    gcc = shutil.which("gcc")
+    if gcc is None:
+        pytest.skip("no C compiler")
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    so = binding.LIB_PATH
+    src = tmp_path / "client.c"
+    src.write_text(C_CLIENT)
+    exe = tmp_path / "client"
+    subprocess.run([gcc, "-std=c99", "-Wall", "-Werror", "-I", os.path.join(root, "include"),
+                    str(src), so, f"-Wl,-rpath,{os.path.dirname(so)}", "-o", str(exe)],
+                   check=True, capture_output=True)
+    out = subprocess.run([str(exe)], check=True, capture_output=True, text=True).stdout.split()
+    assert int(out[0]) == binding.load_library().gqa_version()
+    assert int(out[1]) == binding.load_library().gqa_decode_workspace_bytes(64, 32, 8, 128, 8192)
+    assert int(out[2]) == binding.GQA_ERR_NULL      # null inputs
+    assert int(out[3]) == binding.GQA_ERR_SHAPE     # h_q = 12 is not a multiple of g = 8
+    assert out[4].startswith("GQA_ERR_CACHE_FULL")
