@@ -44,3 +44,30 @@ def decode_flops(seq_lens, h_q: int, d: int) -> int:
 def append_bytes(B: int, T: int, g: int, d: int, elem_bytes: int = 2) -> int:
     """Read T new K and V rows per sequence and write them into the cache."""
     return 2 * 2 * B * T * g * d * elem_bytes
+
+
+def prefill_window_flops(B: int, L: int, h_q: int, d: int, window: int) -> int:
+    """Causal prefill with a sliding window of W keys: query i sees
+    min(i + 1, W) keys."""
+    pairs = sum(min(i + 1, window) for i in range(L))
+    return 4 * B * h_q * d * pairs
+
+
+def prefill_cached_flops(seq_lens, T: int, h_q: int, d: int) -> int:
+    """Chunked prefill of T new tokens per sequence over its cache: new token
+    t of a sequence with n rows sits at position n - T + t and sees
+    n - T + t + 1 keys."""
+    pairs = sum(T * (int(n) - T) + T * (T + 1) // 2 for n in seq_lens)
+    return 4 * h_q * d * pairs
+
+
+def decode_window_kv_bytes(seq_lens, window: int, g: int, d: int, elem_bytes: int = 2) -> int:
+    """K and V bytes of a windowed decode: the last min(len, W) rows."""
+    total_rows = sum(min(int(x), window) for x in seq_lens)
+    return 2 * total_rows * g * d * elem_bytes
+
+
+def rope_append_bytes(B: int, T: int, h_q: int, g: int, d: int, elem_bytes: int = 2) -> int:
+    """Fused RoPE append: read the new query, key and value rows and write the
+    rotated queries and the cache rows (the cos/sin rows are L2-resident)."""
+    return 2 * B * T * (h_q + 2 * g) * d * elem_bytes

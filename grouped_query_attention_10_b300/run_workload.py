@@ -3,7 +3,9 @@
     python -m grouped_query_attention_10_b300.run_workload <name> [--iters N] [--warmup W]
 
 Names: prefill_tiny, prefill_noncausal, prefill_causal, decode_ragged,
-decode_sweep_g{1,2,4,8,16,32}, append_prompt. Inputs are the seeded
+decode_sweep_g{1,2,4,8,16,32}, append_prompt, and the variants prefill_window
+(W = 1024), prefill_alibi, prefill_kvcache (512 new tokens over 4096),
+decode_paged_p{16,64,256}, decode_window (W = 1024), append_rope. Inputs are the seeded
 synthetic workloads of ``inputs.py``. Each timed call is bracketed by CUDA
 events on the launching stream; an L2 flush precedes every call (a 256 MiB
 write, then a 256 MiB read of another buffer, so the write's dirty lines are
@@ -76,6 +78,88 @@ def _append(dev):
     return fn, accounting.append_bytes(w.B, w.L, w.g, w.d), "GB/s", 1e9
 
 
+def _prefill_variant(dev, window=0, alibi=False):
+    """The causal Llama-shape prefill with a sliding window or ALiBi slopes."""
+    w = inputs.LLAMA_CAUSAL_PREFILL
+    q, k, v = inputs.prefill_inputs(w, device=dev)
+    o = torch.empty((w.B, w.L, w.h_q, w.d), dtype=torch.float32, device=dev)
+    slopes = (torch.tensor([2.0 ** (-8.0 * (h + 1) / w.h_q) for h in range(w.h_q)],
+                           dtype=torch.float32, device=dev) if alibi else None)
+    fn = lambda s: gqa.gqa_prefill_fwd(q, k, v, causal=True, scale=w.scale, out=o, stream=s,
+                                       window=window, alibi_slopes=slopes)
+    work = (accounting.prefill_window_flops(w.B, w.L, w.h_q, w.d, window) if window
+            else accounting.prefill_flops(w.B, w.L, w.h_q, w.d, True))
+    return fn, work, "TFLOP/s", 1e12
+
+
+def _prefill_kvcache(dev, T=512):
+    """Chunked prefill: the last T of 4096 tokens per sequence of the Llama
+    shape attend to the whole cache."""
+    w = inputs.LLAMA_CAUSAL_PREFILL
+    q, k, v = inputs.prefill_inputs(w, device=dev)
+    kc = k.transpose(1, 2).contiguous()
+    vc = v.transpose(1, 2).contiguous()
+    qn = q[:, w.L - T:].contiguous()
+    lens = torch.full((w.B,), w.L, dtype=torch.int32, device=dev)
+    o = torch.empty((w.B, T, w.h_q, w.d), dtype=torch.float32, device=dev)
+    fn = lambda s: gqa.gqa_prefill_kvcache_fwd(qn, kc, vc, lens, scale=w.scale, out=o, stream=s)
+    return fn, accounting.prefill_cached_flops([w.L] * w.B, T, w.h_q, w.d), "TFLOP/s", 1e12
+
+
+def _decode_paged(dev, page):
+    """The ragged decode workload through a paged pool (shuffled pages)."""
+    w = inputs.DECODE_RAGGED
+    q, kc, vc, lens = inputs.decode_inputs(w, device=dev)
+    nb = w.S_max // page
+    perm = torch.randperm(w.B * nb, generator=torch.Generator().manual_seed(page))
+    pool_of = lambda c: c.view(w.B, w.g, nb, page, w.d).permute(0, 2, 1, 3, 4).reshape(
+        w.B * nb, w.g, page, w.d)
+    kp = torch.empty_like(kc).view(w.B * nb, w.g, page, w.d)
+    vp = torch.empty_like(kp)
+    kp[perm.to(dev)] = pool_of(kc)
+    vp[perm.to(dev)] = pool_of(vc)
+    table = perm.view(w.B, nb).to(torch.int32).to(dev)
+    del kc, vc
+    o = torch.empty((w.B, w.h_q, w.d), dtype=torch.float32, device=dev)
+    ws = torch.empty(gqa.gqa_decode_paged_workspace_bytes(w.B, w.h_q, w.g, w.d, page, nb),
+                     dtype=torch.uint8, device=dev)
+    fn = lambda s: gqa.gqa_decode_paged_fwd(q, kp, vp, table, lens, scale=w.scale, out=o,
+                                            workspace=ws, stream=s)
+    return fn, accounting.decode_kv_bytes(lens.tolist(), w.g, w.d), "GB/s", 1e9
+
+
+def _decode_window(dev, window=1024):
+    """The ragged decode workload with a sliding window."""
+    w = inputs.DECODE_RAGGED
+    q, kc, vc, lens = inputs.decode_inputs(w, device=dev)
+    o = torch.empty((w.B, w.h_q, w.d), dtype=torch.float32, device=dev)
+    ws = torch.empty(gqa.gqa_decode_workspace_bytes(w.B, w.h_q, w.g, w.d, w.S_max),
+                     dtype=torch.uint8, device=dev)
+    fn = lambda s: gqa.gqa_decode_fwd(q, kc, vc, lens, scale=w.scale, out=o, workspace=ws,
+                                      stream=s, window=window)
+    return fn, accounting.decode_window_kv_bytes(lens.tolist(), window, w.g, w.d), "GB/s", 1e9
+
+
+def _append_rope(dev):
+    """The bench step's prompt (B32 T1024 h8 g4 d64) through the fused RoPE append."""
+    w = inputs.NONCAUSAL_PREFILL
+    q, k, v = inputs.prefill_inputs(w, device=dev)
+    kc = torch.empty((w.B, w.g, w.L, w.d), dtype=torch.bfloat16, device=dev)
+    vc = torch.empty_like(kc)
+    qo = torch.empty_like(q)
+    lens = torch.zeros((w.B,), dtype=torch.int32, device=dev)
+    ang = torch.arange(w.L, dtype=torch.float64)[:, None] * 10000.0 ** (
+        -torch.arange(0, w.d, 2, dtype=torch.float64) / w.d)[None, :]
+    cos = torch.cos(ang).float().to(dev)
+    sin = torch.sin(ang).float().to(dev)
+
+    def fn(s):
+        lens.zero_()
+        gqa.kv_cache_append_rope(kc, vc, lens, k, v, cos, sin, q=q, q_out=qo, stream=s)
+
+    return fn, accounting.rope_append_bytes(w.B, w.L, w.h_q, w.g, w.d), "GB/s", 1e9
+
+
 def make(name: str, dev, B=None):
     if name == "prefill_tiny":
         return _prefill(inputs.TINY_CAUSAL_PREFILL, dev, B)
@@ -89,6 +173,18 @@ def make(name: str, dev, B=None):
         return _decode(inputs.decode_sweep(int(name[len("decode_sweep_g"):])), dev, B)
     if name == "append_prompt":
         return _append(dev)
+    if name == "prefill_window":
+        return _prefill_variant(dev, window=1024)
+    if name == "prefill_alibi":
+        return _prefill_variant(dev, alibi=True)
+    if name == "prefill_kvcache":
+        return _prefill_kvcache(dev)
+    if name.startswith("decode_paged_p"):
+        return _decode_paged(dev, int(name[len("decode_paged_p"):]))
+    if name == "decode_window":
+        return _decode_window(dev)
+    if name == "append_rope":
+        return _append_rope(dev)
     raise SystemExit(f"unknown workload {name}")
 
 
