@@ -36,7 +36,7 @@ METRIC = "GQA prefill TFLOP/s & decode KV-read GB/s vs roofline on 1×B300"
 # DRAM bytes (read + write) of one prefill_kernel<64,false> launch of the bench workload, from
 # the ncu capture summarised in profiles/prefill_noncausal_b32_l1024_hq8_g4_d64.md; reported
 # only while prefill.cu is the source that was profiled (sha256 prefix below).
-PROFILED_PREFILL = {"sha256_prefix": "08d42e410b5bc0a6", "dram_bytes": 67_204_096 + 20_704_512}
+PROFILED_PREFILL = {"sha256_prefix": "041e011e5634ab7f", "dram_bytes": 67_179_008 + 20_607_232}
 FALLBACK_PEAKS = {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0, "bf16_tflops_sustained": 1400.0}
 L2_FLUSH_BYTES = 256 << 20
 

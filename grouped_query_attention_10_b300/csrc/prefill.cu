@@ -531,12 +531,32 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(
                                (kWindow && key0 <= q_abs_last - p.window);
         if (kAlibi) {
           // biased log2-unit scores; masked keys become -inf
+          if (CAUSAL) {
+            // every visible key is at or before the query: the bias of key
+            // key0 + e is b0 + slope * e
+            const float b0 = -slope_log2 * static_cast<float>(q_abs - key0);
+            if (need_mask) {
 #pragma unroll
-          for (int e = 0; e < BN; ++e) {
-            const int key = key0 + e;
-            const float bias = -slope_log2 * static_cast<float>(abs(q_abs - key));
-            const float x = fmaf(__uint_as_float(r[e]), scale_log2, bias);
-            r[e] = __float_as_uint(key > last_key || key < first_key ? -INFINITY : x);
+              for (int e = 0; e < BN; ++e) {
+                const int key = key0 + e;
+                const float x = fmaf(__uint_as_float(r[e]), scale_log2,
+                                     fmaf(slope_log2, static_cast<float>(e), b0));
+                r[e] = __float_as_uint(key > last_key || key < first_key ? -INFINITY : x);
+              }
+            } else {
+#pragma unroll
+              for (int e = 0; e < BN; ++e)
+                r[e] = __float_as_uint(fmaf(__uint_as_float(r[e]), scale_log2,
+                                            fmaf(slope_log2, static_cast<float>(e), b0)));
+            }
+          } else {
+#pragma unroll
+            for (int e = 0; e < BN; ++e) {
+              const int key = key0 + e;
+              const float bias = -slope_log2 * static_cast<float>(abs(q_abs - key));
+              const float x = fmaf(__uint_as_float(r[e]), scale_log2, bias);
+              r[e] = __float_as_uint(key > last_key || key < first_key ? -INFINITY : x);
+            }
           }
         } else if (need_mask) {
 #pragma unroll
