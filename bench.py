@@ -1,17 +1,23 @@
 #!/usr/bin/env python
 """Benchmark of the GQA forward hot path on B300.
 
-One step = one pass of the whole path over one batch of the non-causal
-B=32, L=1024, h_q=8, g=4, d=64 workload (the pages' benchmark shape):
-  1. kv_cache_append  the prompt's K/V (1024 tokens) into a [32, 4, 1025, 64] cache
-  2. gqa_prefill_fwd  non-causal prefill, fp32 output
+One step = one pass of the whole path over one batch of the Llama-style causal
+workload B=4, L=4096, h_q=32, g=8, d=128:
+  1. kv_cache_append  the prompt's K/V (4096 tokens) into a [4, 8, 4097, 128] cache
+  2. gqa_prefill_fwd  causal prefill, fp32 output
   3. kv_cache_append  one new token
-  4. gqa_decode_fwd   one-token decode over the 1025 cached rows
-value = algorithmic FLOPs of the step / device time of the step (TFLOP/s).
-The dominant kernel (prefill) is also timed alone inside each step for the
-roofline figure. After the timed region the script measures, for context,
-the causal B=4 L=4096 h_q=32 g=8 d=128 prefill, the ragged B=64 decode over
-a [64, 8, 8192, 128] cache and the B=16, S=32768 decode group-size sweep.
+  4. gqa_decode_fwd   one-token decode over the 4097 cached rows
+value = algorithmic FLOPs of the step (causal pairs only) / device time of the
+step (TFLOP/s). The dominant kernel (the prefill) is also timed alone inside
+each step for the roofline figure.
+
+The decode half of the metric is measured on the ragged decode workload
+(B=64, h_q=32, g=8, d=128, cache [64, 8, 8192, 128], lengths uniform in
+[1024, 8192]); its KV-read rate and roofline go in ``roofline["decode"]``.
+After that the script measures, for context (``extra``), the pages' non-causal
+benchmark shape B=32 L=1024 h_q=8 g=4 d=64, the B=16 S=32768 decode group-size
+sweep and the variant workloads (sliding window, ALiBi, chunked prefill,
+paged decode, windowed decode, prompt appends).
 
 Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--impl native|reference]
 Under torchrun each rank runs an independent replica on its own GPU.
@@ -20,10 +26,11 @@ Under torchrun each rank runs an independent replica on its own GPU.
 from __future__ import annotations
 
 import argparse
+import hashlib
 import json
-import math
 import os
 import statistics
+import subprocess
 import sys
 import threading
 import time
@@ -33,18 +40,26 @@ if ROOT not in sys.path:
     sys.path.insert(0, ROOT)
 
 METRIC = "GQA prefill TFLOP/s & decode KV-read GB/s vs roofline on 1×B300"
-# DRAM bytes (read + write) of one prefill_kernel<64,false> launch of the bench workload, from
-# the ncu capture summarised in profiles/prefill_noncausal_b32_l1024_hq8_g4_d64.md; reported
-# only while prefill.cu is the source that was profiled (sha256 prefix below).
-PROFILED_PREFILL = {"sha256_prefix": "041e011e5634ab7f", "dram_bytes": 67_179_008 + 20_607_232}
 FALLBACK_PEAKS = {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0, "bf16_tflops_sustained": 1400.0}
-L2_FLUSH_BYTES = 256 << 20
+# Vendor figures, reported beside the measured peaks: dense bf16 tensor rate
+# and HBM3e bandwidth of one B300.
+NOMINAL_BF16_TFLOPS = 2250.0
+NOMINAL_HBM_GBS = 8000.0
+# DRAM bytes (read + write) per launch from the committed ncu captures of the
+# two roofline kernels, valid only while the kernel sources hash to the
+# prefix given (sha256 over the listed files, concatenated in order).
+PROFILED = {
+    "prefill_causal_d128": {"files": ["prefill.cu", "ptx.cuh"], "sha256_prefix": None,
+                            "dram_bytes": None},
+    "decode_ragged": {"files": ["decode.cu", "ptx.cuh"], "sha256_prefix": None,
+                      "dram_bytes": None},
+}
 
 
 def parse_args(argv=None):
     p = argparse.ArgumentParser()
     p.add_argument("--gpus", type=int, default=1)
-    p.add_argument("--steps", type=int, default=1000)
+    p.add_argument("--steps", type=int, default=200)
     p.add_argument("--warmup", type=int, default=5)
     p.add_argument("--impl", choices=["native", "reference"], default="native")
     p.add_argument("--no-extra", action="store_true", help="skip the context measurements")
@@ -112,8 +127,26 @@ def load_peaks():
         return dict(FALLBACK_PEAKS), "fallback"
 
 
+def source_sha(files) -> str:
+    h = hashlib.sha256()
+    for name in files:
+        with open(os.path.join(ROOT, "grouped_query_attention_10_b300", "csrc", name), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()
+
+
+def profiled_traffic(key: str):
+    """ncu DRAM bytes per launch of a roofline kernel, or None when the kernel
+    source has changed since the capture."""
+    p = PROFILED[key]
+    if not p["sha256_prefix"] or p["dram_bytes"] is None:
+        return None
+    return p["dram_bytes"] if source_sha(p["files"]).startswith(p["sha256_prefix"]) else None
+
+
 class ClockSampler:
-    """Samples SM clock and throttle reasons through NVML in a background thread."""
+    """Samples the SM clock and the clock-event reasons with `nvidia-smi -lms`
+    in a child process while the timed region runs."""
 
     REASONS = {
         0x0000000000000001: "gpu_idle",
@@ -126,82 +159,74 @@ class ClockSampler:
         0x0000000000000100: "hw_power_brake_slowdown",
         0x0000000000000200: "display_clock_setting",
     }
+    FIELDS = "clocks.sm,clocks.max.sm,clocks_event_reasons.active"
 
-    def __init__(self, device_index: int, period_s: float = 0.002):
-        self.samples = []
-        self.reasons = 0
-        self.max_mhz = None
-        self.error = None
-        self._stop = threading.Event()
-        self._period = period_s
-        self._ok = False
-        self._device_index = device_index
+    def __init__(self, device_index: int, period_ms: int = 50):
+        self.device = str(device_index)
         try:
-            import pynvml
+            import torch
 
-            pynvml.nvmlInit()
-            self._nv = pynvml
-            self._h = pynvml.nvmlDeviceGetHandleByIndex(device_index)
-            self.max_mhz = pynvml.nvmlDeviceGetMaxClockInfo(self._h, pynvml.NVML_CLOCK_SM)
-            self._ok = True
-        except Exception as e:  # fall back to the nvidia-smi CLI
-            self.error = f"nvml: {type(e).__name__}: {e}"
-            self._ok = False
-
-    def _sample(self):
-        nv = self._nv
-        self.samples.append(nv.nvmlDeviceGetClockInfo(self._h, nv.NVML_CLOCK_SM))
-        try:
-            self.reasons |= nv.nvmlDeviceGetCurrentClocksEventReasons(self._h)
+            uuid = str(torch.cuda.get_device_properties(device_index).uuid)
+            if uuid:
+                self.device = uuid if uuid.startswith("GPU-") else "GPU-" + uuid
         except Exception:
-            self.reasons |= nv.nvmlDeviceGetCurrentClocksThrottleReasons(self._h)
+            pass
+        self.period_ms = period_ms
+        self.proc = None
+        self.lines = []
+        self.error = None
 
-    def _smi_sample(self):
-        import subprocess
-
-        fields = ("clocks.sm,clocks.max.sm,clocks_event_reasons.active")
-        r = subprocess.run(["nvidia-smi", "-i", str(self._device_index),
-                            f"--query-gpu={fields}", "--format=csv,noheader,nounits"],
-                           capture_output=True, text=True, timeout=10)
-        sm, mx, active = [x.strip() for x in r.stdout.strip().split(",")]
-        self.samples.append(float(sm))
-        self.max_mhz = float(mx)
-        self.reasons |= int(active, 16)
-
-    def _run(self):
-        while not self._stop.is_set():
-            try:
-                self._sample() if self._ok else self._smi_sample()
-            except Exception as e:
-                self.error = (self.error or "") + f" sample: {e}"
-                return
-            time.sleep(self._period if self._ok else 0.05)
+    def _query_once(self):
+        r = subprocess.run(["nvidia-smi", "-i", self.device, f"--query-gpu={self.FIELDS}",
+                            "--format=csv,noheader,nounits"], capture_output=True, text=True,
+                           timeout=20)
+        return r.stdout.strip().splitlines()
 
     def __enter__(self):
         try:
-            self._sample() if self._ok else self._smi_sample()
+            self.lines += self._query_once()
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", self.device, f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", str(self.period_ms)],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self._reader = threading.Thread(target=self._read, daemon=True)
+            self._reader.start()
         except Exception as e:
-            self.error = (self.error or "") + f" first sample: {e}"
-        self._t = threading.Thread(target=self._run, daemon=True)
-        self._t.start()
+            self.error = f"nvidia-smi: {type(e).__name__}: {e}"
         return self
 
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
     def __exit__(self, *exc):
-        self._stop.set()
-        self._t.join()
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=10)
+            except Exception:
+                self.proc.kill()
+            self._reader.join(timeout=5)
         try:
-            self._sample() if self._ok else self._smi_sample()
+            self.lines += self._query_once()
         except Exception:
             pass
 
     def summary(self):
-        if not self.samples:
-            return {"sm_mhz": None, "sm_max_mhz": self.max_mhz, "reasons": [],
-                    "samples": 0, "error": self.error}
-        reasons = [name for bit, name in self.REASONS.items() if self.reasons & bit]
-        out = {"sm_mhz": float(statistics.median(self.samples)), "sm_max_mhz": self.max_mhz,
-               "reasons": reasons, "samples": len(self.samples),
-               "source": "nvml" if self._ok else "nvidia-smi"}
+        sm, mx, reasons = [], None, 0
+        for line in self.lines:
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) != 3:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                mx = float(parts[1])
+                reasons |= int(parts[2], 16)
+            except ValueError:
+                continue
+        out = {"sm_mhz": float(statistics.median(sm)) if sm else None, "sm_max_mhz": mx,
+               "reasons": [n for bit, n in self.REASONS.items() if reasons & bit],
+               "samples": len(sm), "source": f"nvidia-smi -lms {self.period_ms}"}
         if self.error:
             out["note"] = self.error
         return out
@@ -219,38 +244,122 @@ def blas_threads() -> int:
     return os.cpu_count() or 1
 
 
+def cpu_model() -> str:
+    try:
+        with open("/proc/cpuinfo") as f:
+            for line in f:
+                if line.startswith("model name"):
+                    return line.split(":", 1)[1].strip()
+    except Exception:
+        pass
+    return "unknown"
+
+
+def _time_calls(fn, n, stream, flush=None):
+    """CUDA-event time of n calls of fn on `stream` (seconds each); the L2
+    flush, when given, runs before every call, outside the timed interval."""
+    import torch
+
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(n)]
+    for a, b in evs:
+        if flush is not None:
+            flush()
+        a.record(stream)
+        fn()
+        b.record(stream)
+    torch.cuda.synchronize()
+    return [a.elapsed_time(b) / 1e3 for a, b in evs]
+
+
 # --------------------------------------------------------------------- CPU oracle legs
 
-def cpu_oracle_prefill_sample(budget_s: float, max_seqs: int = 32):
-    """Time the fp64 oracle on whole sequences of the step's workload."""
-    import numpy as np
+def _group_slice(q, k, v, b, kvh, G):
+    """Sequence b, K/V head kvh and its G query heads, as fp64 arrays."""
+    import torch
+
+    f64 = lambda t: t.to(torch.float64).numpy()
+    return (f64(q[b:b + 1, :, kvh * G:(kvh + 1) * G]), f64(k[b:b + 1, :, kvh:kvh + 1]),
+            f64(v[b:b + 1, :, kvh:kvh + 1]))
+
+
+def oracle_prefill_block(qs, ks, vs, r0, rows, scale):
+    """The oracle on query rows [r0, r0 + rows) of one causal K/V group over
+    keys [0, r0 + rows); returns the FLOPs that block represents."""
+    import oracle
+
+    r1 = min(r0 + rows, qs.shape[1])
+    oracle.prefill(qs[:, r0:r1], ks[:, :r1], vs[:, :r1], True, scale, q_offset=r0)
+    pairs = sum(i + 1 for i in range(r0, r1))
+    return 4 * qs.shape[2] * qs.shape[3] * pairs
+
+
+def cpu_oracle_prefill_sample(budget_s: float, rows: int = 512):
+    """Time the fp64 oracle on whole K/V groups of the causal workload, in
+    blocks of query rows, until the time budget is spent."""
+    from grouped_query_attention_10_b300 import inputs
+
+    w = inputs.LLAMA_CAUSAL_PREFILL
+    q, k, v = inputs.prefill_inputs(w, device="cpu", B=1)
+    G = w.h_q // w.g
+    flops, groups, t0 = 0, 0, time.perf_counter()
+    for kvh in range(w.g):
+        qs, ks, vs = _group_slice(q, k, v, 0, kvh, G)
+        for r0 in range(0, w.L, rows):
+            flops += oracle_prefill_block(qs, ks, vs, r0, rows, w.scale)
+        groups += 1
+        if time.perf_counter() - t0 >= budget_s:
+            break
+    dt = time.perf_counter() - t0
+    return flops / dt / 1e12, groups, dt
+
+
+def cpu_oracle_decode_sample(budget_s: float, max_seqs: int = 64):
+    """Time the fp64 oracle decode on whole sequences of the ragged workload."""
+    import torch
 
     import oracle
     from grouped_query_attention_10_b300 import accounting, inputs
 
-    w = inputs.NONCAUSAL_PREFILL
-    q, k, v = inputs.prefill_inputs(w, device="cpu", B=max_seqs)
-    f64 = lambda t: t.to(__import__("torch").float64).numpy()
-    t0 = time.perf_counter()
-    n = 0
-    while n < max_seqs:
-        oracle.prefill(f64(q[n:n + 1]), f64(k[n:n + 1]), f64(v[n:n + 1]), w.causal, w.scale)
+    w = inputs.DECODE_RAGGED
+    q, kc, vc, lens = inputs.decode_inputs(w, device="cpu", B=8)
+    f64 = lambda t: t.to(torch.float64).numpy()
+    nbytes, n, t0 = 0, 0, time.perf_counter()
+    while n < min(max_seqs, q.shape[0]):
+        L = int(lens[n])
+        oracle.decode(f64(q[n:n + 1]), f64(kc[n:n + 1, :, :L]), f64(vc[n:n + 1, :, :L]), [L],
+                      w.scale)
+        nbytes += accounting.decode_kv_bytes([L], w.g, w.d)
         n += 1
         if time.perf_counter() - t0 >= budget_s:
             break
     dt = time.perf_counter() - t0
-    flops = accounting.prefill_flops(n, w.L, w.h_q, w.d, w.causal)
-    del np
-    return flops / dt / 1e12, n, dt
+    return nbytes / dt / 1e9, n, dt
 
 
 # --------------------------------------------------------------------- native arm
+
+def _step_buffers(w, dev):
+    import torch
+
+    from grouped_query_attention_10_b300 import inputs
+
+    q, k, v = inputs.prefill_inputs(w, device=dev)
+    return {
+        "q": q, "k": k, "v": v,
+        "k_new": inputs.random_bf16((w.B, 1, w.g, w.d), 2001, device=dev),
+        "v_new": inputs.random_bf16((w.B, 1, w.g, w.d), 2002, device=dev),
+        "q_new": inputs.random_bf16((w.B, w.h_q, w.d), 2003, device=dev),
+        "lens0": torch.zeros((w.B,), dtype=torch.int32, device=dev),
+    }
+
 
 def native_arm(args):
     import torch
 
     from grouped_query_attention_10_b300 import accounting, inputs
     from grouped_query_attention_10_b300 import binding as gqa
+    from grouped_query_attention_10_b300.run_workload import make_l2_flush
 
     rank, world, local = dist_env()
     torch.cuda.set_device(local)
@@ -259,13 +368,10 @@ def native_arm(args):
     gqa.load_library()
     peaks, peak_src = load_peaks()
 
-    w = inputs.NONCAUSAL_PREFILL
+    w = inputs.LLAMA_CAUSAL_PREFILL
     B, L, h_q, g, d = w.B, w.L, w.h_q, w.g, w.d
     S_max = L + 1
-    q, k, v = inputs.prefill_inputs(w, device=dev)
-    k_new = inputs.random_bf16((B, 1, g, d), 2001, device=dev)
-    v_new = inputs.random_bf16((B, 1, g, d), 2002, device=dev)
-    q_new = inputs.random_bf16((B, h_q, d), 2003, device=dev)
+    buf = _step_buffers(w, dev)
     kc = torch.empty((B, g, S_max, d), dtype=torch.bfloat16, device=dev)
     vc = torch.empty_like(kc)
     lens = torch.zeros((B,), dtype=torch.int32, device=dev)
@@ -274,31 +380,31 @@ def native_arm(args):
     ws = torch.empty(gqa.gqa_decode_workspace_bytes(B, h_q, g, d, S_max), dtype=torch.uint8,
                      device=dev)
     status = torch.zeros(1, dtype=torch.int32, device=dev)
-    from grouped_query_attention_10_b300.run_workload import make_l2_flush
     flush = make_l2_flush(dev)
     stream = torch.cuda.current_stream(dev)
 
-    flops_prefill = accounting.prefill_flops(B, L, h_q, d, w.causal)
+    flops_prefill = accounting.prefill_flops(B, L, h_q, d, True)
     flops_step = flops_prefill + accounting.decode_flops([S_max] * B, h_q, d)
-    launches_per_step = 2 + 1 + 2 + 2  # append(rows, lens), prefill, append, decode(split, combine)
+    # append (rows + lengths), prefill, append (rows + lengths), decode (split + combine)
+    launches_per_step = 2 + 1 + 2 + 2
 
-    def step_parts(s):
+    def step_parts(s, bf, o_out, od_out):
         # the step in three parts, split where the prefill is timed on its own
         def pre():
             lens.zero_()
-            gqa.kv_cache_append(kc, vc, lens, k, v, status=status, stream=s)
+            gqa.kv_cache_append(kc, vc, lens, bf["k"], bf["v"], status=status, stream=s)
 
         def pf():
-            gqa.gqa_prefill_fwd(q, k, v, causal=w.causal, scale=w.scale, out=o, status=status,
-                                stream=s)
+            gqa.gqa_prefill_fwd(bf["q"], bf["k"], bf["v"], causal=True, scale=w.scale,
+                                out=o_out, status=status, stream=s)
 
         def post():
-            gqa.kv_cache_append(kc, vc, lens, k_new, v_new, status=status, stream=s)
-            gqa.gqa_decode_fwd(q_new, kc, vc, lens, scale=w.scale, out=od, workspace=ws,
-                               status=status, stream=s)
+            gqa.kv_cache_append(kc, vc, lens, bf["k_new"], bf["v_new"], status=status, stream=s)
+            gqa.gqa_decode_fwd(bf["q_new"], kc, vc, lens, scale=w.scale, out=od_out,
+                               workspace=ws, status=status, stream=s)
         return pre, pf, post
 
-    eager_parts = step_parts(stream)
+    eager_parts = step_parts(stream, buf, o, od)
 
     def step():
         for fn in eager_parts:
@@ -311,13 +417,13 @@ def native_arm(args):
     o_eager, od_eager = o.clone(), od.clone()
 
     # The timed steps replay the same library calls captured as CUDA graphs
-    # (the launches of the small append / decode kernels then follow each
-    # other without host round trips); the results must equal the eager ones.
+    # (the small append / decode launches then follow each other without host
+    # round trips); the results must equal the eager ones bit for bit.
     cap = torch.cuda.Stream(dev)
     cap.wait_stream(stream)
     graphs = []
     with torch.cuda.stream(cap):
-        for fn in step_parts(cap):
+        for fn in step_parts(cap, buf, o, od):
             gr = torch.cuda.CUDAGraph()
             with torch.cuda.graph(gr, stream=cap):
                 fn()
@@ -363,53 +469,31 @@ def native_arm(args):
     value = units / t_max / 1e12
     ms_per_step = t_max * 1e3 / args.steps
 
-    import hashlib
-
-    src = os.path.join(ROOT, "grouped_query_attention_10_b300", "csrc", "prefill.cu")
-    with open(src, "rb") as f:
-        same_kernel = hashlib.sha256(f.read()).hexdigest().startswith(
-            PROFILED_PREFILL["sha256_prefix"])
     prefill_s = statistics.mean(prefill_ms) / 1e3
     achieved = flops_prefill / prefill_s / 1e12
-    roofline = {"bound": "tensor", "kernel": "prefill_kernel<64,false>",
-                "achieved": round(achieved, 2), "peak": peaks["bf16_tflops"],
-                "unit": "TFLOP/s", "frac": round(achieved / peaks["bf16_tflops"], 4),
-                "peak_source": f"{peak_src} bf16 dense burst",
-                "traffic": PROFILED_PREFILL["dram_bytes"] if same_kernel else None,
-                "traffic_unit": "bytes per launch (ncu dram read+write)",
-                "algorithmic_bytes": accounting.prefill_bytes(B, L, h_q, g, d, 4)}
+    roofline = {
+        "bound": "tensor", "kernel": "prefill_kernel<128,causal>",
+        "achieved": round(achieved, 2), "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
+        "frac": round(achieved / peaks["bf16_tflops"], 4),
+        "peak_source": f"{peak_src} bf16 dense burst (cuBLAS)",
+        "nominal_peak": NOMINAL_BF16_TFLOPS,
+        "frac_of_nominal": round(achieved / NOMINAL_BF16_TFLOPS, 4),
+        "frac_of_sustained": round(achieved / peaks["bf16_tflops_sustained"], 4),
+        "traffic": profiled_traffic("prefill_causal_d128"),
+        "traffic_unit": "bytes per launch (ncu dram read+write)",
+        "algorithmic_bytes": accounting.prefill_bytes(B, L, h_q, g, d, 4),
+        "algorithmic_flops": flops_prefill,
+        "launch_ms": round(prefill_s * 1e3, 4),
+        "timed": f"CUDA events around the prefill inside each of the {args.steps} steps",
+    }
+    del o_eager, od_eager
+    torch.cuda.empty_cache()
 
-    # ---- end to end: pinned host inputs in, results back, copies timed
-    pin = lambda t: t.detach().to("cpu").pin_memory()
-    h_in = [pin(x) for x in (q, k, v, k_new, v_new, q_new)]
-    d_in = [q, k, v, k_new, v_new, q_new]
-    h_o = torch.empty(o.shape, dtype=o.dtype, pin_memory=True)
-    h_od = torch.empty(od.shape, dtype=od.dtype, pin_memory=True)
-    h2d = sum(x.numel() * x.element_size() for x in h_in)
-    d2h = o.numel() * o.element_size() + od.numel() * od.element_size()
+    roofline["decode"] = decode_roofline(dev, stream, peaks, peak_src, flush)
+    torch.cuda.empty_cache()
 
-    def e2e_step():
-        for hd, dd in zip(h_in, d_in):
-            dd.copy_(hd, non_blocking=True)
-        step()
-        h_o.copy_(o, non_blocking=True)
-        h_od.copy_(od, non_blocking=True)
-
-    for _ in range(3):
-        e2e_step()
-    torch.cuda.synchronize()
-    e2e_evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-               for _ in range(args.steps)]
-    barrier()
-    for a, b_ in e2e_evs:
-        a.record(stream)
-        e2e_step()
-        b_.record(stream)
-    torch.cuda.synchronize()
-    e2e_t = reduce_max(sum(a.elapsed_time(b_) for a, b_ in e2e_evs) / 1e3, dev)
-    e2e = {"value": round(units / e2e_t / 1e12, 3), "unit": "TFLOP/s",
-           "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-           "ms_per_step": round(e2e_t * 1e3 / args.steps, 4)}
+    e2e = e2e_pipelined(args, dev, w, kc, vc, lens, ws, status, flops_step)
+    torch.cuda.empty_cache()
 
     result = {
         "metric": METRIC,
@@ -423,13 +507,16 @@ def native_arm(args):
         "scaling": "weak",
         "vs_baseline": None,
         "dtype": "bf16",
-        "data": "synthetic",
-        "config": {"workload": "gqa_step_noncausal_b32_l1024_hq8_g4_d64",
-                   "B": B, "L": L, "h_q": h_q, "g": g, "d": d, "causal": False,
-                   "step": "append prompt K/V, prefill, append 1 token, decode 1 token",
+        "data": "synthetic (seeded N(0,1) bf16)",
+        "config": {"workload": w.name,
+                   "B": B, "L": L, "h_q": h_q, "g": g, "d": d, "causal": True,
+                   "out": "fp32",
+                   "step": "append prompt K/V, causal prefill, append 1 token, decode 1 token",
+                   "flops": "causal pairs only: 4*B*h_q*d*L(L+1)/2 + decode 4*B*h_q*d*(L+1)",
                    "l2": "flushed between timed steps (256 MiB write, then 256 MiB read)",
                    "launch": "each step replays three CUDA graphs of the library calls "
-                             "(reset + prompt append | prefill | token append + decode)",
+                             "(length reset + prompt append | prefill | token append + decode)",
+                   "decode_workload": inputs.DECODE_RAGGED.name,
                    "parallelism": f"replicas x{world}"},
         "roofline": roofline,
         "e2e": e2e,
@@ -439,111 +526,199 @@ def native_arm(args):
 
     if rank == 0 and world == 1:
         budget = float(os.environ.get("GQA_BENCH_CPU_BUDGET_S", "12"))
-        tf, nseq, dt = cpu_oracle_prefill_sample(budget)
+        tf, groups, dt = cpu_oracle_prefill_sample(budget)
+        gbs, nseq, dtd = cpu_oracle_decode_sample(budget / 2)
         result["cpu_baseline"] = {
             "value": tf, "unit": "TFLOP/s", "cores": blas_threads(), "kind": "oracle",
-            "sample": f"fp64 NumPy oracle prefill on {nseq} of the 32 sequences "
-                      f"({dt:.1f} s); decode and append not included"}
+            "cpu": cpu_model(),
+            "sample": f"fp64 NumPy oracle, causal prefill of {groups} of the 32 K/V groups "
+                      f"(4 query heads x 4096 rows each, blocks of 512 rows; {dt:.1f} s)",
+            "decode": {"value": round(gbs, 4), "unit": "GB/s", "kind": "oracle",
+                       "sample": f"fp64 NumPy oracle decode of {nseq} ragged sequences "
+                                 f"of the decode workload ({dtd:.1f} s)"},
+        }
     if not args.no_extra:
-        result["extra"] = extra_measurements(dev, stream, peaks, peak_src)
+        result["extra"] = extra_measurements(dev, stream, peaks, peak_src, flush)
     if rank == 0:
         print(json.dumps(result), flush=True)
 
 
-def _time_calls(fn, n, stream, flush=None):
-    import torch
-
-    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-           for _ in range(n)]
-    for a, b in evs:
-        if flush is not None:
-            flush()
-        a.record(stream)
-        fn()
-        b.record(stream)
-    torch.cuda.synchronize()
-    return [a.elapsed_time(b) / 1e3 for a, b in evs]
-
-
-def extra_measurements(dev, stream, peaks, peak_src):
-    """Context measurements on the other workloads (not part of `value`)."""
+def decode_roofline(dev, stream, peaks, peak_src, flush, n_calls=60):
+    """KV-read rate of the ragged decode workload (split + combine launches),
+    against the measured HBM copy rate and the nominal HBM figure."""
     import torch
 
     from grouped_query_attention_10_b300 import accounting, inputs
     from grouped_query_attention_10_b300 import binding as gqa
 
+    w = inputs.DECODE_RAGGED
+    q, kc, vc, lens = inputs.decode_inputs(w, device=dev)
+    o = torch.empty((w.B, w.h_q, w.d), dtype=torch.float32, device=dev)
+    ws = torch.empty(gqa.gqa_decode_workspace_bytes(w.B, w.h_q, w.g, w.d, w.S_max),
+                     dtype=torch.uint8, device=dev)
+    fn = lambda: gqa.gqa_decode_fwd(q, kc, vc, lens, scale=w.scale, out=o, workspace=ws,
+                                    stream=stream)
+    _time_calls(fn, 5, stream, flush)
+    ts = _time_calls(fn, n_calls, stream, flush)
+    nbytes = accounting.decode_kv_bytes(lens.tolist(), w.g, w.d)
+    t = statistics.mean(ts)
+    gbs = nbytes / t / 1e9
+    block = {
+        "bound": "hbm", "kernel": "decode_split_kernel<128,1> + decode_combine_kernel<128>",
+        "workload": w.name, "achieved": round(gbs, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
+        "frac": round(gbs / peaks["hbm_gbs"], 4),
+        "peak_source": f"{peak_src} HBM copy rate (read+write bytes)",
+        "nominal_peak": NOMINAL_HBM_GBS, "frac_of_nominal": round(gbs / NOMINAL_HBM_GBS, 4),
+        "traffic": profiled_traffic("decode_ragged"),
+        "traffic_unit": "bytes per launch of decode_split_kernel (ncu dram read+write)",
+        "algorithmic_bytes": nbytes, "launch_us": round(t * 1e6, 2),
+        "median_us": round(statistics.median(ts) * 1e6, 2),
+        "timed": f"CUDA events, mean of {n_calls} calls, L2 flushed before each",
+    }
+    return block
+
+
+def e2e_pipelined(args, dev, w, kc, vc, lens, ws, status, flops_step):
+    """The step through the public API with the inputs in pinned host memory
+    and the outputs read back every step: host->device copies, the library
+    calls and device->host copies run on three streams, two steps in flight."""
+    import torch
+
+    from grouped_query_attention_10_b300 import binding as gqa
+
+    B, L, h_q, d = w.B, w.L, w.h_q, w.d
+    host_src = _step_buffers(w, "cpu")
+    h_in = {k: t.pin_memory() for k, t in host_src.items()}
+    d_in = [{k: torch.empty_like(t, device=dev) for k, t in h_in.items()} for _ in range(2)]
+    d_o = [torch.empty((B, L, h_q, d), dtype=torch.float32, device=dev) for _ in range(2)]
+    d_od = [torch.empty((B, h_q, d), dtype=torch.float32, device=dev) for _ in range(2)]
+    h_o = [torch.empty((B, L, h_q, d), dtype=torch.float32, pin_memory=True) for _ in range(2)]
+    h_od = [torch.empty((B, h_q, d), dtype=torch.float32, pin_memory=True) for _ in range(2)]
+    h2d = sum(t.numel() * t.element_size() for t in h_in.values())
+    d2h = d_o[0].numel() * 4 + d_od[0].numel() * 4
+    s_in, s_comp, s_out = (torch.cuda.Stream(dev) for _ in range(3))
+    in_ready = [torch.cuda.Event() for _ in range(2)]
+    comp_done = [torch.cuda.Event() for _ in range(2)]
+    out_done = [torch.cuda.Event() for _ in range(2)]
+    torch.cuda.synchronize()
+    for e in comp_done + out_done:
+        e.record(s_comp)
+
+    def run(n):
+        for i in range(n):
+            sl = i % 2
+            s_in.wait_event(comp_done[sl])  # step i-2 no longer reads this slot's inputs
+            with torch.cuda.stream(s_in):
+                for k, t in h_in.items():
+                    d_in[sl][k].copy_(t, non_blocking=True)
+            in_ready[sl].record(s_in)
+            s_comp.wait_event(in_ready[sl])
+            s_comp.wait_event(out_done[sl])  # step i-2's outputs have been read back
+            bf = d_in[sl]
+            with torch.cuda.stream(s_comp):
+                lens.copy_(bf["lens0"], non_blocking=True)
+            gqa.kv_cache_append(kc, vc, lens, bf["k"], bf["v"], status=status, stream=s_comp)
+            gqa.gqa_prefill_fwd(bf["q"], bf["k"], bf["v"], causal=True, scale=w.scale,
+                                out=d_o[sl], status=status, stream=s_comp)
+            gqa.kv_cache_append(kc, vc, lens, bf["k_new"], bf["v_new"], status=status,
+                                stream=s_comp)
+            gqa.gqa_decode_fwd(bf["q_new"], kc, vc, lens, scale=w.scale, out=d_od[sl],
+                               workspace=ws, status=status, stream=s_comp)
+            comp_done[sl].record(s_comp)
+            s_out.wait_event(comp_done[sl])
+            with torch.cuda.stream(s_out):
+                h_o[sl].copy_(d_o[sl], non_blocking=True)
+                h_od[sl].copy_(d_od[sl], non_blocking=True)
+            out_done[sl].record(s_out)
+
+    run(3)
+    torch.cuda.synchronize()
+    n = max(args.steps // 4, 8)
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    barrier()
+    torch.cuda.synchronize()
+    t0.record(s_in)
+    run(n)
+    s_out.wait_stream(s_in)
+    s_out.wait_stream(s_comp)
+    t1.record(s_out)
+    torch.cuda.synchronize()
+    e2e_t = reduce_max(t0.elapsed_time(t1) / 1e3, dev)
+    units = reduce_sum(flops_step * n, dev)
+    return {"value": round(units / e2e_t / 1e12, 3), "unit": "TFLOP/s",
+            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+            "ms_per_step": round(e2e_t * 1e3 / n, 4), "steps": n,
+            "how": "public API calls on a compute stream; pinned host->device copies of each "
+                   "step's inputs and device->host copies of O and the decode output on two "
+                   "copy streams, two steps in flight"}
+
+
+def extra_measurements(dev, stream, peaks, peak_src, flush):
+    """Context measurements on the other workloads (not part of `value`)."""
+    import torch
+
+    from grouped_query_attention_10_b300 import run_workload
+
     out = {}
-    # causal Llama-style prefill; inputs + output exceed L2
-    w = inputs.LLAMA_CAUSAL_PREFILL
-    q, k, v = inputs.prefill_inputs(w, device=dev)
-    o = torch.empty((w.B, w.L, w.h_q, w.d), dtype=torch.float32, device=dev)
-    fn = lambda: gqa.gqa_prefill_fwd(q, k, v, causal=True, scale=w.scale, out=o, stream=stream)
-    _time_calls(fn, 3, stream)
-    ts = _time_calls(fn, 10, stream)
-    flops = accounting.prefill_flops(w.B, w.L, w.h_q, w.d, True)
-    tf = flops / statistics.median(ts) / 1e12
-    out[w.name] = {"tflops": round(tf, 2), "ms": round(statistics.median(ts) * 1e3, 4),
-                   "frac_of_bf16_peak": round(tf / peaks["bf16_tflops"], 4),
-                   "peak_source": peak_src}
-    del q, k, v, o
-    torch.cuda.empty_cache()
 
-    def decode_case(w):
-        q, kc, vc, lens = inputs.decode_inputs(w, device=dev)
-        o = torch.empty((w.B, w.h_q, w.d), dtype=torch.float32, device=dev)
-        ws = torch.empty(gqa.gqa_decode_workspace_bytes(w.B, w.h_q, w.g, w.d, w.S_max),
-                         dtype=torch.uint8, device=dev)
-        from grouped_query_attention_10_b300.run_workload import make_l2_flush
-        flush = make_l2_flush(dev)
-        fn = lambda: gqa.gqa_decode_fwd(q, kc, vc, lens, scale=w.scale, out=o, workspace=ws,
-                                        stream=stream)
-        _time_calls(fn, 3, stream, flush)
-        ts = _time_calls(fn, 10, stream, flush)
-        nbytes = accounting.decode_kv_bytes(lens.tolist(), w.g, w.d)
-        t = statistics.median(ts)
-        gbs = nbytes / t / 1e9
-        return {"gbs": round(gbs, 1), "us": round(t * 1e6, 2), "kv_bytes": nbytes,
-                "frac_of_hbm": round(gbs / peaks["hbm_gbs"], 4), "peak_source": peak_src}
-
-    out[inputs.DECODE_RAGGED.name] = decode_case(inputs.DECODE_RAGGED)
-    torch.cuda.empty_cache()
-    sweep = {}
-    for g in inputs.DECODE_SWEEP_G:
-        sweep[f"g{g}"] = decode_case(inputs.decode_sweep(g))
+    def one(name, n=20, peak=None, nominal=None):
+        fn, work, unit, div = run_workload.make(name, dev)
+        call = lambda: fn(stream)
+        _time_calls(call, 3, stream, flush)
+        ts = _time_calls(call, n, stream, flush)
+        t = statistics.mean(ts)
+        rate = work / t / div
+        rec = {"rate": round(rate, 2), "unit": unit, "us": round(t * 1e6, 2)}
+        if unit == "TFLOP/s":
+            rec["frac_of_bf16_peak"] = round(rate / peaks["bf16_tflops"], 4)
+            rec["frac_of_nominal"] = round(rate / NOMINAL_BF16_TFLOPS, 4)
+        else:
+            rec["frac_of_hbm"] = round(rate / peaks["hbm_gbs"], 4)
+            rec["frac_of_nominal"] = round(rate / NOMINAL_HBM_GBS, 4)
+        rec["peak_source"] = peak_src
+        del fn
         torch.cuda.empty_cache()
-    out["decode_sweep_b16_hq32_d128_s32768"] = sweep
+        return rec
+
+    out["prefill_noncausal_b32_l1024_hq8_g4_d64"] = one("prefill_noncausal", 50)
+    for g in (1, 2, 4, 8, 16, 32):
+        out[f"decode_sweep_b16_hq32_g{g}_d128_s32768"] = one(f"decode_sweep_g{g}", 20)
+    for name in ("prefill_window", "prefill_alibi", "prefill_kvcache", "decode_paged_p16",
+                 "decode_paged_p64", "decode_window", "append_prompt", "append_rope"):
+        out[name] = one(name, 20)
     return out
 
 
 # --------------------------------------------------------------------- reference arm
 
 def reference_arm(args):
-    """The CPU oracle, timed as it stands, on bounded samples of the workload."""
-    import torch
-
-    import oracle
-    from grouped_query_attention_10_b300 import accounting, inputs
+    """The CPU oracle, timed as it stands, on bounded samples of the workload:
+    each step is one block of 256 query rows of one causal K/V group."""
+    from grouped_query_attention_10_b300 import inputs
 
     rank, world, _ = dist_env()
     if rank != 0:
         return
-    w = inputs.NONCAUSAL_PREFILL
-    n_seq = 4
-    q, k, v = inputs.prefill_inputs(w, device="cpu", B=n_seq)
-    f64 = lambda t: t.to(torch.float64).numpy()
-    qs, ks, vs = f64(q), f64(k), f64(v)
+    w = inputs.LLAMA_CAUSAL_PREFILL
+    G = w.h_q // w.g
+    rows = 256
+    q, k, v = inputs.prefill_inputs(w, device="cpu", B=1)
+    groups = [_group_slice(q, k, v, 0, kvh, G) for kvh in range(2)]
+    blocks = [(gi, r0) for gi in range(len(groups)) for r0 in range(0, w.L, rows)]
 
     def step(i):
-        b = i % n_seq
-        oracle.prefill(qs[b:b + 1], ks[b:b + 1], vs[b:b + 1], w.causal, w.scale)
+        gi, r0 = blocks[i % len(blocks)]
+        qs, ks, vs = groups[gi]
+        return oracle_prefill_block(qs, ks, vs, r0, rows, w.scale)
 
     for i in range(max(args.warmup, 1)):
         step(i)
     t0 = time.perf_counter()
+    flops = 0
     for i in range(args.steps):
-        step(i)
+        flops += step(i)
     dt = time.perf_counter() - t0
-    flops = accounting.prefill_flops(1, w.L, w.h_q, w.d, w.causal) * args.steps
     value = flops / dt / 1e12
     line = {
         "impl": "reference",
@@ -558,14 +733,14 @@ def reference_arm(args):
         "scaling": "weak",
         "vs_baseline": None,
         "dtype": "f64",
-        "data": "synthetic",
-        "config": {"workload": "gqa_step_noncausal_b32_l1024_hq8_g4_d64", "B": w.B, "L": w.L,
-                   "h_q": w.h_q, "g": w.g, "d": w.d, "causal": False,
-                   "parallelism": "cpu, rank 0 only"},
+        "data": "synthetic (seeded N(0,1) bf16)",
+        "config": {"workload": w.name, "B": w.B, "L": w.L, "h_q": w.h_q, "g": w.g, "d": w.d,
+                   "causal": True, "parallelism": "cpu, rank 0 only"},
         "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": blas_threads(),
-                         "kind": "oracle",
-                         "sample": "fp64 NumPy oracle prefill of one sequence "
-                                   "(8 heads x 1024 x 1024) per step"},
+                         "kind": "oracle", "cpu": cpu_model(),
+                         "sample": f"fp64 NumPy oracle, one block of {rows} causal query rows "
+                                   f"of one K/V group ({G} query heads) per step, cycling "
+                                   "over the rows of two groups"},
         "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
                 "d2h_bytes_per_step": 0},
     }

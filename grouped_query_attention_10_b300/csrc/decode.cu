@@ -576,37 +576,21 @@ int decode_split_len(int B, int h_q, int g, int S_max) {
   return static_cast<int>(l);
 }
 
-namespace {
-
-int decode_sm_count() {
-  static int n = 0;
-  if (n == 0) {
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess ||
-        cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n < 1)
-      n = 148;
-  }
-  return n;
-}
-
-}  // namespace
-
 template <int D, int MT>
 static cudaError_t launch_decode_t(const DecodeArgs& a, cudaStream_t s) {
   constexpr int kSmem = DecCfg<D>::kSmem;
-  static bool attr_set = false;
-  if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(decode_split_kernel<D, MT>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
-    if (e != cudaSuccess) return e;
-    attr_set = true;
-  }
+  static DeviceOnce attr_once;
+  cudaError_t e = run_once_per_device(attr_once, [] {
+    return cudaFuncSetAttribute(decode_split_kernel<D, MT>,
+                                cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
+  });
+  if (e != cudaSuccess) return e;
   const int n_hslice = (a.G + 31) / 32;
   const long long n_items = static_cast<long long>(a.B) * a.g * n_hslice * a.n_split;
-  const long long slots = static_cast<long long>(decode_sm_count()) * kCtasPerSm;
+  const long long slots = static_cast<long long>(device_sm_count()) * kCtasPerSm;
   const int grid = static_cast<int>(n_items < slots ? n_items : slots);
   // the item counter the persistent CTAs fetch from starts at zero
-  cudaError_t e = cudaMemsetAsync(a.item_counter, 0, sizeof(int), s);
+  e = cudaMemsetAsync(a.item_counter, 0, sizeof(int), s);
   if (e != cudaSuccess) return e;
   decode_split_kernel<D, MT><<<grid, kThreads, kSmem, s>>>(
       a.tm_k, a.tm_v, static_cast<const __nv_bfloat16*>(a.q), a.seq_lens, a.part_o, a.part_lse,

@@ -4,10 +4,52 @@
 
 #include <cuda.h>
 #include <cuda_runtime.h>
+
+#include <atomic>
 #include <cstddef>
 #include <cstdint>
+#include <mutex>
 
 namespace gqa {
+
+// Devices a process may drive through this library (ordinals 0 .. 63).
+constexpr int kMaxDevices = 64;
+
+// One-time set-up that must happen on every device the library launches on
+// (a kernel's dynamic shared-memory opt-in is a per-device attribute). Safe to
+// call from several host threads; a set-up that failed is tried again on the
+// next call.
+struct DeviceOnce {
+  std::mutex mu;
+  std::atomic<bool> done[kMaxDevices] = {};
+};
+
+template <typename F>
+cudaError_t run_once_per_device(DeviceOnce& once, F setup) {
+  int dev = -1;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+  if (once.done[dev].load(std::memory_order_acquire)) return cudaSuccess;
+  std::lock_guard<std::mutex> lock(once.mu);
+  if (once.done[dev].load(std::memory_order_relaxed)) return cudaSuccess;
+  e = setup();
+  if (e == cudaSuccess) once.done[dev].store(true, std::memory_order_release);
+  return e;
+}
+
+// Streaming multiprocessors of the current device (looked up once per device).
+inline int device_sm_count() {
+  static std::atomic<int> count[kMaxDevices] = {};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return 148;
+  int n = count[dev].load(std::memory_order_relaxed);
+  if (n > 0) return n;
+  if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n < 1)
+    return 148;
+  count[dev].store(n, std::memory_order_relaxed);
+  return n;
+}
 
 // Rows of one prefill query tile (TMEM lanes) and keys per K/V tile.
 constexpr int kPrefillBM = 128;

@@ -763,40 +763,25 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(
   if (threadIdx.x == 0 && abort_flag) record_status(p.status, GQA_ERR_TIMEOUT);
 }
 
-namespace {
-
-int sm_count() {
-  static int n = 0;  // one device per process in practice; re-queried if unset
-  if (n == 0) {
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess ||
-        cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n < 1)
-      n = 148;
-  }
-  return n;
-}
-
-}  // namespace
-
 template <int D, bool CAUSAL, int VAR>
 static cudaError_t launch_prefill_t(const PrefillArgs& a, cudaStream_t s) {
   constexpr uint32_t kSmem = PrefillCfg<D>::kSmem;
-  static bool attr_set = false;
-  if (!attr_set) {
+  static DeviceOnce attr_once;
+  cudaError_t e = run_once_per_device(attr_once, [] {
     // the register hand-over inside the kernel assumes the launch pool
     cudaFuncAttributes fa{};
-    cudaError_t e = cudaFuncGetAttributes(&fa, prefill_kernel<D, CAUSAL, VAR>);
-    if (e != cudaSuccess) return e;
+    cudaError_t r = cudaFuncGetAttributes(&fa, prefill_kernel<D, CAUSAL, VAR>);
+    if (r != cudaSuccess) return r;
     if (fa.numRegs != kRegsLaunch) return cudaErrorInvalidKernelImage;
-    e = cudaFuncSetAttribute(prefill_kernel<D, CAUSAL, VAR>,
-                             cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
-    if (e != cudaSuccess) return e;
-    attr_set = true;
-  }
+    return cudaFuncSetAttribute(prefill_kernel<D, CAUSAL, VAR>,
+                                cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
+  });
+  if (e != cudaSuccess) return e;
   const int PM = BM / a.G;
   const int n_ctiles = (a.Lq + 2 * PM - 1) / (2 * PM);
   const long long n_units = static_cast<long long>(n_ctiles) * a.g * a.B;
-  const int grid = static_cast<int>(n_units < sm_count() ? n_units : sm_count());
+  const int n_sm = device_sm_count();
+  const int grid = static_cast<int>(n_units < n_sm ? n_units : n_sm);
   PrefillParams p{};
   p.lse = a.lse;
   p.o_dtype = a.o_dtype;

@@ -30,6 +30,14 @@
  *    (prefill) and their products fit the index types (B*L*h_q*d < 2^31,
  *    B*g*S_max < 2^31).
  *  - Kernels are built for sm_103a only; another device yields GQA_ERR_CUDA.
+ *
+ * Where these declarations differ from the interface as first specified:
+ * every entry point returns int (a gqa_status_t value) and gqa_status_string
+ * takes int, so FFI callers see a fixed 32-bit type whatever width a C
+ * compiler picks for the enum; the output arguments (o, o_dtype, lse) sit
+ * together right after the inputs, before the sizes; and every launching
+ * entry point takes the optional device status word status_dev, the only
+ * channel through which a kernel can report a run-time problem.
  */
 #ifndef GQA_B300_H
 #define GQA_B300_H

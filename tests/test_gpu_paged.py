@@ -3,7 +3,8 @@
 Paged decode and paged append through the C interface against the fp64
 oracle's paged functions (which are pinned to the contiguous ones), on
 shuffled physical pages, ragged lengths, page sizes below and above the
-64-token decode stage, and with the window / ALiBi options.
+64-token decode stage, and with the window / ALiBi options. Outputs and page
+pools sit between NaN guard bands that every call must leave untouched.
 """
 
 import math
@@ -12,6 +13,7 @@ import numpy as np
 import pytest
 import torch
 
+import guard
 import oracle
 from grouped_query_attention_10_b300 import binding as gqa
 from grouped_query_attention_10_b300 import inputs
@@ -63,11 +65,16 @@ def test_paged_decode_matches_oracle(page, h_q, g, d):
     lens = [2048, 1, 777, 1500]
     q, kp, vp, table_t, table = paged_case(B, h_q, g, d, page, max_blocks, lens, 11 + page + g)
     lens_t = torch.tensor(lens, dtype=torch.int32, device=DEV)
-    lse = torch.empty((B, h_q), dtype=torch.float32, device=DEV)
+    gl = guard.empty((B, h_q), torch.float32, DEV)
+    go = guard.empty((B, h_q, d), torch.float32, DEV)
+    lse = gl.tensor
     status = torch.zeros(1, dtype=torch.int32, device=DEV)
-    o = gqa.gqa_decode_paged_fwd(q, kp, vp, table_t, lens_t, lse=lse, status=status)
+    o = gqa.gqa_decode_paged_fwd(q, kp, vp, table_t, lens_t, lse=lse, status=status,
+                                 out=go.tensor)
     torch.cuda.synchronize()
     assert int(status.item()) == 0
+    go.assert_bands(f"paged decode O page={page}")
+    gl.assert_bands(f"paged decode lse page={page}")
     scale = 1.0 / math.sqrt(d)
     o_ref, lse_ref = oracle.decode_paged(f64(q), f64(kp), f64(vp), table, lens, page, scale)
     assert_close(f64(o), o_ref, f"paged decode page={page}")
@@ -129,9 +136,13 @@ def test_paged_append_bit_exact_then_decode(page):
     bits = lambda t: t.view(torch.int16).cpu().numpy()
     k_ref, v_ref, lens_ref, st_ref = oracle.append_paged(bits(kp), bits(vp), table, lens0,
                                                          bits(kn), bits(vn), page)
+    gk, gv = guard.copy_of(kp), guard.copy_of(vp)
+    kp, vp = gk.tensor, gv.tensor
     status = torch.zeros(1, dtype=torch.int32, device=DEV)
     gqa.kv_cache_append_paged(kp, vp, table_t, lens, kn, vn, status=status)
     torch.cuda.synchronize()
+    gk.assert_bands(f"paged append K pool page={page}")
+    gv.assert_bands(f"paged append V pool page={page}")
     assert np.array_equal(bits(kp), k_ref) and np.array_equal(bits(vp), v_ref)
     assert list(lens.cpu().numpy()) == list(lens_ref)
     assert int(status.item()) == st_ref == oracle.APPEND_CACHE_FULL

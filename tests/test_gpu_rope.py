@@ -14,6 +14,7 @@ import numpy as np
 import pytest
 import torch
 
+import guard
 import oracle
 from grouped_query_attention_10_b300 import binding as gqa
 from grouped_query_attention_10_b300 import inputs
@@ -64,10 +65,19 @@ def test_rope_append_bit_exact(d, h_q, g, in_place):
         bits(kc), bits(vc), lens0, bits(kn), bits(vn), cos, sin, q=bits(q_before),
         q_out=bits(q_out_before))
     lens = torch.tensor(lens0, dtype=torch.int32, device=DEV)
+    gk, gv = guard.copy_of(kc), guard.copy_of(vc)
+    kc, vc = gk.tensor, gv.tensor
+    if not in_place:
+        gq = guard.copy_of(q_out)
+        q_out = gq.tensor
     status = torch.zeros(1, dtype=torch.int32, device=DEV)
     res = gqa.kv_cache_append_rope(kc, vc, lens, kn, vn, dev(cos), dev(sin), q=q, q_out=q_out,
                                    status=status)
     torch.cuda.synchronize()
+    gk.assert_bands("RoPE append K cache")
+    gv.assert_bands("RoPE append V cache")
+    if not in_place:
+        gq.assert_bands("RoPE append rotated queries")
     assert res is q_out
     assert int(status.item()) == st_ref == oracle.APPEND_CACHE_FULL
     assert list(lens.cpu().numpy()) == list(l_ref)
@@ -118,10 +128,14 @@ def test_paged_rope_append_bit_exact(page):
     k_ref, v_ref, l_ref, st_ref, q_ref = oracle.append_paged_rope(
         bits(kp), bits(vp), table, lens0, bits(kn), bits(vn), page, cos, sin, q=bits(q))
     lens = torch.tensor(lens0, dtype=torch.int32, device=DEV)
+    gk, gv = guard.copy_of(kp), guard.copy_of(vp)
+    kp, vp = gk.tensor, gv.tensor
     status = torch.zeros(1, dtype=torch.int32, device=DEV)
     gqa.kv_cache_append_paged_rope(kp, vp, dev(table), lens, kn, vn, dev(cos), dev(sin), q=q,
                                    status=status)
     torch.cuda.synchronize()
+    gk.assert_bands(f"paged RoPE append K pool page={page}")
+    gv.assert_bands(f"paged RoPE append V pool page={page}")
     assert int(status.item()) == st_ref == oracle.APPEND_CACHE_FULL
     assert list(lens.cpu().numpy()) == list(l_ref)
     assert np.array_equal(bits(kp), k_ref)

@@ -4,7 +4,8 @@ Sliding window and ALiBi (the variants the pages name) on prefill and
 decode, and the chunked prefill in which T new tokens attend to a
 [B, g, S_max, d] KV cache, all through the C interface against the fp64
 oracle on the same seeded bf16 inputs. Tolerance as in the other parity
-tests: max abs error <= 1e-2, mean abs error <= 1e-3.
+tests: max abs error <= 1e-2, mean abs error <= 1e-3, for O and for lse.
+Output and lse buffers sit between NaN guard bands that must stay untouched.
 """
 
 import math
@@ -13,6 +14,7 @@ import numpy as np
 import pytest
 import torch
 
+import guard
 import oracle
 from grouped_query_attention_10_b300 import binding as gqa
 from grouped_query_attention_10_b300 import inputs
@@ -62,9 +64,14 @@ def test_prefill_sliding_window(d, L, window):
     k = rand_bf16((B, L, g, d), 301 + L)
     v = rand_bf16((B, L, g, d), 302 + L)
     scale = 1.0 / math.sqrt(d)
-    lse = torch.empty((B, h_q, L), dtype=torch.float32, device=DEV)
-    o = gqa.gqa_prefill_fwd(q, k, v, causal=True, scale=scale, window=window, lse=lse)
+    go = guard.empty((B, L, h_q, d), torch.float32, DEV)
+    gl = guard.empty((B, h_q, L), torch.float32, DEV)
+    lse = gl.tensor
+    o = gqa.gqa_prefill_fwd(q, k, v, causal=True, scale=scale, window=window, lse=lse,
+                            out=go.tensor)
     torch.cuda.synchronize()
+    go.assert_bands(f"windowed prefill O L={L}")
+    gl.assert_bands(f"windowed prefill lse L={L}")
     o_ref, lse_ref = oracle.prefill(f64(q), f64(k), f64(v), True, scale, window=window)
     assert_close(f64(o), o_ref, f"window {window} L={L} d={d}")
     assert_close(f64(lse), lse_ref, "lse")
@@ -80,13 +87,18 @@ def test_prefill_alibi(d, causal, h_q, g):
     v = rand_bf16((B, L, g, d), 402 + h_q + g)
     scale = 1.0 / math.sqrt(d)
     slopes = alibi_slopes(h_q)
-    lse = torch.empty((B, h_q, L), dtype=torch.float32, device=DEV)
-    o = gqa.gqa_prefill_fwd(q, k, v, causal=causal, scale=scale, alibi_slopes=slopes, lse=lse)
+    go = guard.empty((B, L, h_q, d), torch.float32, DEV)
+    gl = guard.empty((B, h_q, L), torch.float32, DEV)
+    lse = gl.tensor
+    o = gqa.gqa_prefill_fwd(q, k, v, causal=causal, scale=scale, alibi_slopes=slopes, lse=lse,
+                            out=go.tensor)
     torch.cuda.synchronize()
+    go.assert_bands("ALiBi prefill O")
+    gl.assert_bands("ALiBi prefill lse")
     o_ref, lse_ref = oracle.prefill(f64(q), f64(k), f64(v), causal, scale,
                                     alibi_slopes=slopes.cpu().numpy().astype(np.float64))
     assert_close(f64(o), o_ref, f"alibi causal={causal} h_q={h_q} g={g}")
-    assert_close(f64(lse), lse_ref, "lse", max_abs=2e-2)
+    assert_close(f64(lse), lse_ref, "lse")
 
 
 def test_prefill_window_and_alibi_llama_shape_sampled_rows():
@@ -134,12 +146,16 @@ def _cached_case(B, T, h_q, g, d, S_max, lens, seed, window=0, alibi=False, nan_
             vc[b, :, n:] = float("nan")
     slopes = alibi_slopes(h_q) if alibi else None
     scale = 1.0 / math.sqrt(d)
-    lse = torch.empty((B, h_q, T), dtype=torch.float32, device=DEV)
+    go = guard.empty((B, T, h_q, d), torch.float32, DEV)
+    gl = guard.empty((B, h_q, T), torch.float32, DEV)
+    lse = gl.tensor
     status = torch.zeros(1, dtype=torch.int32, device=DEV)
     o = gqa.gqa_prefill_kvcache_fwd(q, kc, vc, lens_t, scale=scale, lse=lse, window=window,
-                                    alibi_slopes=slopes, status=status)
+                                    alibi_slopes=slopes, status=status, out=go.tensor)
     torch.cuda.synchronize()
     assert int(status.item()) == 0
+    go.assert_bands(f"chunked prefill O T={T}")
+    gl.assert_bands(f"chunked prefill lse T={T}")
     sl = None if slopes is None else slopes.cpu().numpy().astype(np.float64)
     kc64 = np.nan_to_num(f64(kc))  # rows past the length are never visible to the oracle
     vc64 = np.nan_to_num(f64(vc))
@@ -164,7 +180,7 @@ def test_prefill_kvcache_variants(h_q, g, window, alibi):
     o, lse, o_ref, lse_ref = _cached_case(2, 100, h_q, g, 128, 900, [900, 333], seed=700 + h_q,
                                           window=window, alibi=alibi)
     assert_close(f64(o), o_ref, f"kvcache window={window} alibi={alibi}")
-    assert_close(f64(lse), lse_ref, "lse", max_abs=2e-2)
+    assert_close(f64(lse), lse_ref, "lse")
 
 
 def test_append_then_chunked_prefill_then_decode_pipeline():
@@ -226,17 +242,21 @@ def test_decode_window_alibi(G_cfg, window, alibi):
             kc[b, :, :lo] = float("nan")
             vc[b, :, :lo] = float("nan")
     slopes = alibi_slopes(h_q) if alibi else None
-    lse = torch.empty((B, h_q), dtype=torch.float32, device=DEV)
+    gl = guard.empty((B, h_q), torch.float32, DEV)
+    go = guard.empty((B, h_q, d), torch.float32, DEV)
+    lse = gl.tensor
     status = torch.zeros(1, dtype=torch.int32, device=DEV)
     o = gqa.gqa_decode_fwd(q, kc, vc, lens, scale=0.0884, lse=lse, window=window,
-                           alibi_slopes=slopes, status=status)
+                           alibi_slopes=slopes, status=status, out=go.tensor)
     torch.cuda.synchronize()
     assert int(status.item()) == 0
+    go.assert_bands("windowed decode O")
+    gl.assert_bands("windowed decode lse")
     sl = None if slopes is None else slopes.cpu().numpy().astype(np.float64)
     o_ref, lse_ref = oracle.decode(f64(q), np.nan_to_num(f64(kc)), np.nan_to_num(f64(vc)),
                                    lens_l, 0.0884, window=window, alibi_slopes=sl)
     assert_close(f64(o), o_ref, f"decode window={window} alibi={alibi}")
-    assert_close(f64(lse), lse_ref, "lse", max_abs=2e-2)
+    assert_close(f64(lse), lse_ref, "lse")
 
 
 def test_decode_equals_one_token_chunked_prefill_with_bias():
