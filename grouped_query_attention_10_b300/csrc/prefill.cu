@@ -26,9 +26,10 @@
 // Warp roles (384 threads):
 //   warp 0        TMA producer: query tiles, then K and V tiles through
 //                 shared-memory rings
-//   warp 1        TMEM allocator + tcgen05.mma issuer of query tile 0
-//   warp 2        tcgen05.mma issuer of query tile 1 (each issuer warp walks
-//                 the schedule, one elected lane issues)
+//   warp 1        TMEM allocator + tcgen05.mma issuer (d = 64: of query
+//                 tile 0; d = 128: of both query tiles, in a fixed order)
+//   warp 2        d = 64: tcgen05.mma issuer of query tile 1 (each issuer
+//                 warp walks the schedule, one elected lane issues)
 //   warps 4..7    softmax + epilogue of query tile 0 (warp w owns TMEM lanes
 //                 32*(w%4)..)
 //   warps 8..11   softmax + epilogue of query tile 1
@@ -40,8 +41,17 @@
 //    the tensor core while the exponentials of tile j are computed.
 //  * d = 128: S and O fill TMEM, so P_t overwrites the first 64 columns of
 //    S_t and S_t(j+1) is issued after P_t(j).V_j (one thread issues all of
-//    tile t's MMAs, and tcgen05 MMAs from one thread execute in order).
+//    tile t's MMAs, and tcgen05 MMAs from one thread execute in order). The
+//    softmax hands P_t over in two halves (keys 0..63, then 64..127), so the
+//    first half of P_t.V runs while the second half's exponentials are
+//    computed.
 // While the softmax of one tile runs, the tensor core works on the other.
+//
+// Every K (V) ring slot is released by a commit issued right after the last
+// score (P.V) product that reads it, so the producer can refill it as soon
+// as that product retires; with the 2-deep rings of d = 128 a release one
+// product later left the next K tile still in flight when its score product
+// was due.
 //
 // The online softmax keeps a running row max in log2 units and rescales O
 // lazily: only when some row's max grew by more than 2^8 (exact either way,
@@ -69,7 +79,7 @@ constexpr float kRescaleThreshold = 8.0f;  // log2 units
 // kernel uses exactly kRegsLaunch registers, so the increase always finds
 // the registers the decrease released.
 constexpr int kRegsLaunch = 168;
-constexpr int kRegsCtl = 80;
+constexpr int kRegsCtl = 88;
 constexpr int kRegsSoftmax = 208;
 static_assert(128 * kRegsCtl + 256 * kRegsSoftmax <= kThreads * kRegsLaunch,
               "register plan exceeds the launch pool");
@@ -210,7 +220,8 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(
   __shared__ __align__(8) uint64_t bar_ve[VS];
   __shared__ __align__(8) uint64_t bar_s[2];    // S_t in TMEM
   __shared__ __align__(8) uint64_t bar_sf[2];   // S_t read by the softmax (separate-P only)
-  __shared__ __align__(8) uint64_t bar_p[2];    // P_t written to TMEM (and O_t rescaled)
+  __shared__ __align__(8) uint64_t bar_p[2];    // P_t (d = 128: its first half) in TMEM, O_t rescaled
+  __shared__ __align__(8) uint64_t bar_p2[2];   // d = 128: second half of P_t in TMEM
   __shared__ __align__(8) uint64_t bar_o[2];    // P_t.V retired
   __shared__ __align__(8) uint64_t bar_fin[2];  // every MMA of issuer t retired
   __shared__ __align__(8) uint64_t bar_stw[2];  // output stage t written (128 arrivals)
@@ -225,23 +236,26 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(
 
   if (threadIdx.x == 0) {
     abort_flag = 0;
-    // empty barriers take one arrival from each of the two MMA issuers
+    // empty barriers take one arrival from each MMA issuer (two at d = 64,
+    // one issuing for both tiles at d = 128)
+    constexpr uint32_t kIssuers = kSepP ? 2 : 1;
     for (int i = 0; i < NQ; ++i) {
       mbar_init(&bar_q[i], 1);
-      mbar_init(&bar_qe[i], 2);
+      mbar_init(&bar_qe[i], kIssuers);
     }
     for (int i = 0; i < KS; ++i) {
       mbar_init(&bar_kf[i], 1);
-      mbar_init(&bar_ke[i], 2);
+      mbar_init(&bar_ke[i], kIssuers);
     }
     for (int i = 0; i < VS; ++i) {
       mbar_init(&bar_vf[i], 1);
-      mbar_init(&bar_ve[i], 2);
+      mbar_init(&bar_ve[i], kIssuers);
     }
     for (int t = 0; t < 2; ++t) {
       mbar_init(&bar_s[t], 1);
       mbar_init(&bar_sf[t], 128);
       mbar_init(&bar_p[t], 128);
+      mbar_init(&bar_p2[t], 128);
       mbar_init(&bar_o[t], 1);
     }
     mbar_init(&bar_fin[0], 1);
@@ -327,44 +341,39 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(
     }
   } else if (warp <= 2) {
     // ------------------------------------------------------------ MMA issuers
-    // Warp 1 + t issues every MMA of query tile t, so the two tiles' chains
-    // (S_t -> softmax -> P_t.V) never wait on each other's hand-offs. The
-    // whole warp walks the schedule (it stays converged and keeps the
-    // descriptors in uniform registers); one elected lane issues. A K/V ring
-    // slot (and the query slot) is released once BOTH issuers are done with
-    // it: the empty barriers count two arrivals, a commit from an issuer that
-    // used the slot or a plain arrive from one that did not.
-    const int t = warp - 1;
+    // The whole issuing warp walks the schedule (it stays converged and keeps
+    // the descriptors in uniform registers); one elected lane issues.
     const bool leader = elect_one();
     const uint32_t sbase = smem_u32(smem);
     // descriptor bases; a k-step only moves the 14-bit start-address field
-    const uint64_t dq0 = smem_desc_sw128(sbase + t * C::kQTile, 16, 1024);
+    const uint64_t dq0 = smem_desc_sw128(sbase, 16, 1024);
     const uint64_t dk0 = smem_desc_sw128(sbase + C::kOffK, 16, 1024);
     const uint64_t dv0 = smem_desc_sw128(sbase + C::kOffV, BN * 128, 1024);
-    const uint32_t d_s = tmem + static_cast<uint32_t>(t) * BN;
-    const uint32_t p_t = tmem + C::kColP + static_cast<uint32_t>(t) * C::kStrideP;
-    const uint32_t o_t = tmem + C::kColO + static_cast<uint32_t>(t) * D;
     // byte offset (>> 4) of k-step kk inside a K-major 128-byte-swizzled tile
     auto kmaj = [](int kk) -> uint64_t {
       return static_cast<uint64_t>(((kk >> 2) * (BM * 128) + (kk & 3) * 32) >> 4);
     };
-    auto issue_s = [&](int qs, int ks) {
-      const uint64_t aq = dq0 + static_cast<uint64_t>((qs * C::kQSlot) >> 4);
+    // S_t = Q_t K^T for query tile t (query slot qs, K ring slot ks)
+    auto issue_s = [&](int t, int qs, int ks) {
+      const uint64_t aq = dq0 + static_cast<uint64_t>((qs * C::kQSlot + t * C::kQTile) >> 4);
       const uint64_t bk = dk0 + static_cast<uint64_t>((ks * C::kKVStage) >> 4);
+      const uint32_t d_s = tmem + static_cast<uint32_t>(t) * BN;
 #pragma unroll
       for (int kk = 0; kk < D / 16; ++kk)
         mma_bf16_ss(d_s, aq + kmaj(kk), bk + kmaj(kk), kIdescS, kk > 0 ? 1u : 0u);
       mma_commit(&bar_s[t]);
     };
-    auto issue_pv = [&](int vs, bool first) {
-      // V tile [BN keys x D], D contiguous: MN-major B operand; LBO = distance
-      // between the 64-wide column blocks of D; a k-step is 16 rows of 128 B
+    // O_t += P_t V over the keys of k-steps [k0, k1) (16 keys each). V tile
+    // [BN keys x D], D contiguous: MN-major B operand; LBO = distance between
+    // the 64-wide column blocks of D; a k-step is 16 rows of 128 B
+    auto issue_pv = [&](int t, int vs, bool first, int k0, int k1) {
       const uint64_t bv = dv0 + static_cast<uint64_t>((vs * C::kKVStage) >> 4);
+      const uint32_t p_t = tmem + C::kColP + static_cast<uint32_t>(t) * C::kStrideP;
+      const uint32_t o_t = tmem + C::kColO + static_cast<uint32_t>(t) * D;
 #pragma unroll
-      for (int kk = 0; kk < BN / 16; ++kk)
+      for (int kk = k0; kk < k1; ++kk)
         mma_bf16_ts(o_t, p_t + kk * 8, bv + static_cast<uint64_t>((kk * 16 * 128) >> 4),
                     kIdescO, (!first || kk > 0) ? 1u : 0u);
-      mma_commit(&bar_o[t]);
     };
     auto wait_all = [&](uint64_t* bar, uint32_t parity) {
       return __all_sync(0xffffffffu, mbar_wait(bar, parity, &abort_flag));
@@ -380,95 +389,157 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(
       __syncwarp();
     };
 
-    int nu = 0, kb = 0;  // units and K/V tiles (of all units) consumed so far
-    int it = 0;          // (unit, K/V tile) steps of this query tile so far
-    bool ok = true;
-    for (int u = blockIdx.x; u < n_units && ok; u += gridDim.x, ++nu) {
-      const Unit w = decode_unit(u, p, PM, CAUSAL, kWindow, kCache);
-      const int n_kv = max(w.n0, w.n1);
-      const int n_me = t == 0 ? w.n0 : w.n1;
-      const int qs = nu % NQ;
-      if (n_me > 0) {
-        ok = wait_all(&bar_q[qs], (nu / NQ) & 1);
-        if (ok) ok = wait_all(&bar_kf[kb % KS], (kb / KS) & 1);
-        // S_t(0): with separate P the softmax must have read the previous S_t;
-        // with P inside S_t, the previous P_t.V was issued before (in order)
-        if (ok && kSepP && it > 0) ok = wait_all(&bar_sf[t], (it - 1) & 1);
-        if (!ok) break;
-        tc_fence_after();
-        if (leader) issue_s(qs, kb % KS);
-        __syncwarp();
-      }
-      // the query slot is free once this tile's last score product retires;
-      // a tile without keys gives it back only once it has landed (a plain
-      // arrive must never run ahead of the fill it releases)
-      if (n_me == 0) {
-        ok = wait_all(&bar_q[qs], (nu / NQ) & 1);
-        if (!ok) break;
-      }
-      if (n_me <= 1) release(&bar_qe[qs], n_me == 1);
-      for (int j = 0; ok && j < n_kv; ++j) {
-        const int kj = kb + j;  // ring index of K/V tile j
-        if (j >= n_me) {
-          // this query tile sees no keys from tile j on: give the slots back,
-          // each only after its fill has landed, so this issuer can never
-          // arrive twice on a slot before the other issuer has used it
-          ok = wait_all(&bar_kf[kj % KS], (kj / KS) & 1);
+    if (kSepP) {
+      // d = 64: warp 1 + t issues every MMA of query tile t, so the two
+      // tiles' chains (S_t -> softmax -> P_t.V) never wait on each other's
+      // hand-offs. A K/V ring slot (and the query slot) is released once BOTH
+      // issuers are done with it: the empty barriers count two arrivals, a
+      // commit from an issuer that used the slot or a plain arrive from one
+      // that did not.
+      const int t = warp - 1;
+      int nu = 0, kb = 0;  // units and K/V tiles (of all units) consumed so far
+      int it = 0;          // (unit, K/V tile) steps of this query tile so far
+      bool ok = true;
+      for (int u = blockIdx.x; u < n_units && ok; u += gridDim.x, ++nu) {
+        const Unit w = decode_unit(u, p, PM, CAUSAL, kWindow, kCache);
+        const int n_kv = max(w.n0, w.n1);
+        const int n_me = t == 0 ? w.n0 : w.n1;
+        const int qs = nu % NQ;
+        if (n_me > 0) {
+          ok = wait_all(&bar_q[qs], (nu / NQ) & 1);
+          if (ok) ok = wait_all(&bar_kf[kb % KS], (kb / KS) & 1);
+          // S_t(0) once the softmax has read the previous S_t
+          if (ok && it > 0) ok = wait_all(&bar_sf[t], (it - 1) & 1);
           if (!ok) break;
-          release(&bar_ke[kj % KS], false);
-          ok = wait_all(&bar_vf[kj % VS], (kj / VS) & 1);
-          if (!ok) break;
-          release(&bar_ve[kj % VS], false);
-          continue;
+          tc_fence_after();
+          if (leader) issue_s(t, qs, kb % KS);
+          __syncwarp();
+          release(&bar_ke[kb % KS], true);  // K tile 0: its only reader is issued
         }
-        const bool more = j + 1 < n_me;
-        if (kSepP) {
-          // K tile j: its score product was issued last step
-          release(&bar_ke[kj % KS], true);
-          if (more) {
+        // the query slot is free once this tile's last score product retires;
+        // a tile without keys gives it back only once it has landed (a plain
+        // arrive must never run ahead of the fill it releases)
+        if (n_me == 0) {
+          ok = wait_all(&bar_q[qs], (nu / NQ) & 1);
+          if (!ok) break;
+        }
+        if (n_me <= 1) release(&bar_qe[qs], n_me == 1);
+        for (int j = 0; ok && j < n_kv; ++j) {
+          const int kj = kb + j;  // ring index of K/V tile j
+          if (j >= n_me) {
+            // this query tile sees no keys from tile j on: give the slots
+            // back, each only after its fill has landed, so this issuer can
+            // never arrive twice on a slot before the other issuer has used it
+            ok = wait_all(&bar_kf[kj % KS], (kj / KS) & 1);
+            if (!ok) break;
+            release(&bar_ke[kj % KS], false);
+            ok = wait_all(&bar_vf[kj % VS], (kj / VS) & 1);
+            if (!ok) break;
+            release(&bar_ve[kj % VS], false);
+            continue;
+          }
+          if (j + 1 < n_me) {
             // S_t(j+1) as soon as the softmax has read S_t(j)
             ok = wait_all(&bar_kf[(kj + 1) % KS], ((kj + 1) / KS) & 1);
             if (ok) ok = wait_all(&bar_sf[t], (it + j) & 1);
             if (!ok) break;
             tc_fence_after();
-            if (leader) issue_s(qs, (kj + 1) % KS);
+            if (leader) issue_s(t, qs, (kj + 1) % KS);
             __syncwarp();
+            release(&bar_ke[(kj + 1) % KS], true);
             if (j + 2 == n_me) release(&bar_qe[qs], true);
           }
           ok = wait_all(&bar_vf[kj % VS], (kj / VS) & 1);
           if (ok) ok = wait_all(&bar_p[t], (it + j) & 1);
           if (!ok) break;
           tc_fence_after();
-          if (leader) issue_pv(kj % VS, j == 0);
-          __syncwarp();
-          release(&bar_ve[kj % VS], true);
-        } else {
-          // P_t(j) lives in S_t: P_t(j).V_j first, then S_t(j+1)
-          ok = wait_all(&bar_vf[kj % VS], (kj / VS) & 1);
-          if (ok) ok = wait_all(&bar_p[t], (it + j) & 1);
-          if (ok && more) ok = wait_all(&bar_kf[(kj + 1) % KS], ((kj + 1) / KS) & 1);
-          if (!ok) break;
-          tc_fence_after();
           if (leader) {
-            issue_pv(kj % VS, j == 0);
-            if (more) issue_s(qs, (kj + 1) % KS);
+            issue_pv(t, kj % VS, j == 0, 0, BN / 16);
+            mma_commit(&bar_o[t]);
           }
           __syncwarp();
-          if (more && j + 2 == n_me) release(&bar_qe[qs], true);
-          release(&bar_ke[kj % KS], true);
           release(&bar_ve[kj % VS], true);
         }
+        if (!ok) break;
+        kb += n_kv;
+        it += n_me;
       }
-      if (!ok) break;
-      kb += n_kv;
-      it += n_me;
+      // every MMA must have retired before TMEM is released
+      if (leader) {
+        mma_commit(&bar_fin[t]);
+        mbar_drain(&bar_fin[t], 0);
+      }
+      __syncwarp();
+    } else if (warp == 1) {
+      // d = 128: P_t(j) lives in S_t, so S_t(j+1) can only follow P_t(j).V_j.
+      // One warp issues the MMAs of both query tiles, tile 0's work of a step
+      // before tile 1's. The tensor core executes them in that order, so one
+      // tile's next scores are ready a whole batch (P.V + S, ~1000 cycles)
+      // before the other's and the two softmax warpgroups take turns with the
+      // tensor core. (Two issuers let the tensor core interleave the two
+      // batches; both tiles' scores then finished together and the softmax
+      // warpgroups ran side by side while the tensor core idled.) Each ring
+      // slot has one release, a commit issued right after its last reader.
+      int nu = 0, kb = 0;       // units and K/V tiles (of all units) consumed so far
+      int it0 = 0, it1 = 0;     // (unit, K/V tile) steps of query tile 0 / 1 so far
+      bool ok = true;
+      for (int u = blockIdx.x; u < n_units && ok; u += gridDim.x, ++nu) {
+        const Unit w = decode_unit(u, p, PM, CAUSAL, kWindow, kCache);
+        const int n_kv = max(w.n0, w.n1);  // w.n0 >= 1: tile 0 always sees a key tile
+        const int qs = nu % NQ;
+        ok = wait_all(&bar_q[qs], (nu / NQ) & 1);
+        if (ok) ok = wait_all(&bar_kf[kb % KS], (kb / KS) & 1);
+        if (!ok) break;
+        tc_fence_after();
+        if (leader) {
+          issue_s(0, qs, kb % KS);
+          if (w.n1 > 0) issue_s(1, qs, kb % KS);
+        }
+        __syncwarp();
+        release(&bar_ke[kb % KS], true);
+        if (n_kv == 1) release(&bar_qe[qs], true);
+        for (int j = 0; ok && j < n_kv; ++j) {
+          const int kj = kb + j;  // ring index of K/V tile j
+          ok = wait_all(&bar_vf[kj % VS], (kj / VS) & 1);
+#pragma unroll
+          for (int t = 0; t < 2; ++t) {
+            const int n_t = t == 0 ? w.n0 : w.n1;
+            const int ph = ((t == 0 ? it0 : it1) + j) & 1;
+            if (!ok || j >= n_t) continue;
+            // keys 0..63 as soon as their half of P_t(j) is written
+            ok = wait_all(&bar_p[t], ph);
+            if (!ok) break;
+            tc_fence_after();
+            if (leader) issue_pv(t, kj % VS, j == 0, 0, BN / 32);
+            __syncwarp();
+            ok = wait_all(&bar_p2[t], ph);
+            if (ok && j + 1 < n_t) ok = wait_all(&bar_kf[(kj + 1) % KS], ((kj + 1) / KS) & 1);
+            if (!ok) break;
+            tc_fence_after();
+            if (leader) {
+              issue_pv(t, kj % VS, j == 0, BN / 32, BN / 16);
+              mma_commit(&bar_o[t]);
+              if (j + 1 < n_t) issue_s(t, qs, (kj + 1) % KS);
+            }
+            __syncwarp();
+          }
+          if (!ok) break;
+          release(&bar_ve[kj % VS], true);               // both tiles' P.V_j issued
+          if (j + 1 < n_kv) release(&bar_ke[(kj + 1) % KS], true);  // both S(j+1) issued
+          if (j + 2 == n_kv) release(&bar_qe[qs], true);  // the unit's last S issued
+        }
+        if (!ok) break;
+        kb += n_kv;
+        it0 += w.n0;
+        it1 += w.n1;
+      }
+      // every MMA must have retired before TMEM is released
+      if (leader) {
+        mma_commit(&bar_fin[0]);
+        mbar_drain(&bar_fin[0], 0);
+      }
+      __syncwarp();
     }
-    // every MMA must have retired before TMEM is released
-    if (leader) {
-      mma_commit(&bar_fin[t]);
-      mbar_drain(&bar_fin[t], 0);
-    }
-    __syncwarp();
   }
   } else {
     setmaxnreg_inc<kRegsSoftmax>();
@@ -518,8 +589,12 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(
         if (!ok) break;
         tc_fence_after();
         uint32_t r[BN];
+        if (D == 128) {
+          tmem_ld128(t_s, r);  // one instruction: measured faster than four x32 loads here
+        } else {
 #pragma unroll
-        for (int c = 0; c < BN / 32; ++c) tmem_ld32(t_s + c * 32, r + c * 32);
+          for (int c = 0; c < BN / 32; ++c) tmem_ld32(t_s + c * 32, r + c * 32);
+        }
         tmem_ld_wait();
         if (kSepP) {
           // S_t may be overwritten by the next score product from here on
@@ -600,14 +675,35 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(
             }
           }
         }
-        // The two softmax warps that share an SM sub-partition (warp 4+q of
-        // tile 0, warp 8+q of tile 1) take turns on the exponential unit, in
-        // the order (step j, tile 0), (step j, tile 1), (step j+1, tile 0)...:
-        // one warp's exponentials overlap the other's loads, max and waits
-        // instead of both halving each other's throughput. Phase k waits for
-        // phase k-1 (of either warp; phase k+1 cannot have started).
+        if (kCache && key0 + BN > w.Lk) {
+          // cache rows past the sequence may hold anything (even NaN) and
+          // 0 * NaN would poison P.V: zero them in this V stage (both query
+          // tiles may write the same zeros) once the stage has landed, before
+          // any part of P_t(j) is handed to the tensor core
+          const int vslot = (kvbase + j) % VS;
+          ok = __all_sync(0xffffffffu, mbar_wait(&bar_vf[vslot], ((kvbase + j) / VS) & 1,
+                                                  &abort_flag));
+          if (!ok) break;
+          uint8_t* vst = smem + C::kOffV + vslot * C::kKVStage;
+          const int r_lo = max(0, w.Lk - key0);
+          for (int i = threadIdx.x - 128 - 128 * t; i < (BN - r_lo) * (D / 64) * 8; i += 128) {
+            const int rr = r_lo + i / ((D / 64) * 8);
+            const int cb = (i / 8) % (D / 64);
+            *reinterpret_cast<uint4*>(vst + cb * (BN * 128) + rr * 128 + (i % 8) * 16) =
+                make_uint4(0u, 0u, 0u, 0u);
+          }
+          fence_proxy_async_smem();  // visible to the tensor core's reads of V
+        }
+        // d = 64: the two softmax warps that share an SM sub-partition (warp
+        // 4+q of tile 0, warp 8+q of tile 1) take turns on the exponential
+        // unit, in the order (step j, tile 0), (step j, tile 1), (step j+1,
+        // tile 0)...: one warp's exponentials overlap the other's loads, max
+        // and waits instead of both halving each other's throughput. Phase k
+        // waits for phase k-1 (of either warp; phase k+1 cannot have started).
+        // At d = 128 the two tiles' steps are already staggered by their
+        // score products and the turns only add waits.
         const int kt = kturn + min(j, w.n0) + min(j, w.n1) + (t == 1 && j < w.n0 ? 1 : 0);
-        if (kt > 0) {
+        if (kSepP && kt > 0) {
           ok = mbar_wait(&bar_turn[wq], (kt - 1) & 1, &abort_flag);
           ok = __all_sync(0xffffffffu, ok);
           if (!ok) break;
@@ -640,29 +736,18 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(
             }
           }
           tmem_st32(t_p + hh * 32, pw);  // P columns [32hh, 32hh+32) = keys [64hh, 64hh+64)
-        }
-        mbar_arrive(&bar_turn[wq]);  // this warp's exponential phase is over
-        if (kCache && key0 + BN > w.Lk) {
-          // cache rows past the sequence may hold anything (even NaN) and
-          // 0 * NaN would poison P.V: zero them in this V stage (both query
-          // tiles may write the same zeros) once the stage has landed
-          const int vslot = (kvbase + j) % VS;
-          ok = __all_sync(0xffffffffu, mbar_wait(&bar_vf[vslot], ((kvbase + j) / VS) & 1,
-                                                  &abort_flag));
-          if (!ok) break;
-          uint8_t* vst = smem + C::kOffV + vslot * C::kKVStage;
-          const int r_lo = max(0, w.Lk - key0);
-          for (int i = threadIdx.x - 128 - 128 * t; i < (BN - r_lo) * (D / 64) * 8; i += 128) {
-            const int rr = r_lo + i / ((D / 64) * 8);
-            const int cb = (i / 8) % (D / 64);
-            *reinterpret_cast<uint4*>(vst + cb * (BN * 128) + rr * 128 + (i % 8) * 16) =
-                make_uint4(0u, 0u, 0u, 0u);
+          if (!kSepP && hh == 0) {
+            // d = 128: keys 0..63 of P_t(j) (and the rescaled O_t) go to the
+            // tensor core while the second half is computed
+            tmem_st_wait();
+            tc_fence_before();
+            mbar_arrive(&bar_p[t]);
           }
-          fence_proxy_async_smem();  // visible to the tensor core's reads of V
         }
+        if (kSepP) mbar_arrive(&bar_turn[wq]);  // this warp's exponential phase is over
         tmem_st_wait();
         tc_fence_before();
-        mbar_arrive(&bar_p[t]);
+        mbar_arrive(kSepP ? &bar_p[t] : &bar_p2[t]);
         float a0, a1, b0, b1;
         split_f32x2(sum2[0], a0, a1);
         split_f32x2(sum2[1], b0, b1);
@@ -689,6 +774,14 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(
       // k = the stage is free again after pass k, bar_stw[t] phase k = every
       // thread has written its rows for pass k
       for (int c0 = 0; c0 < n_chunks && ok; c0 += C::kStageChunks, ++npass) {
+        // this pass's accumulator columns, read from TMEM before waiting for
+        // the stage (fp32: kStageChunks chunks of 32 columns; bf16: one chunk
+        // of 64 columns)
+        uint32_t v[64];
+        tmem_ld32(t_o + (f32 ? c0 * 32 : c0 * 64), v);
+        if (!f32 || C::kStageChunks == 2)
+          tmem_ld32(t_o + (f32 ? c0 * 32 + 32 : c0 * 64 + 32), v + 32);
+        tmem_ld_wait();
         if (npass > 0) {
           if (wg_leader) {
             bulk_wait_read_all();  // the previous pass's stores have read the stage
@@ -697,39 +790,29 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(
           ok = mbar_wait(&bar_stf[t], (npass - 1) & 1, &abort_flag);
           if (!ok) break;
         }
+        if (f32) {
 #pragma unroll
-        for (int cc = 0; cc < C::kStageChunks; ++cc) {
-          const int chunk = c0 + cc;
-          if (chunk >= n_chunks) break;
-          uint8_t* dst = stage + cc * C::kChunkBytes + row * 128;
-          if (f32) {
-            uint32_t rr[32];
-            tmem_ld32(t_o + chunk * 32, rr);
-            tmem_ld_wait();
+          for (int cc = 0; cc < C::kStageChunks; ++cc) {
+            uint8_t* dst = stage + cc * C::kChunkBytes + row * 128;
 #pragma unroll
             for (int u4 = 0; u4 < 8; ++u4)
               *reinterpret_cast<float4*>(dst + ((u4 ^ sw) << 4)) =
-                  make_float4(__uint_as_float(rr[4 * u4]) * inv_l,
-                              __uint_as_float(rr[4 * u4 + 1]) * inv_l,
-                              __uint_as_float(rr[4 * u4 + 2]) * inv_l,
-                              __uint_as_float(rr[4 * u4 + 3]) * inv_l);
-          } else {
+                  make_float4(__uint_as_float(v[32 * cc + 4 * u4]) * inv_l,
+                              __uint_as_float(v[32 * cc + 4 * u4 + 1]) * inv_l,
+                              __uint_as_float(v[32 * cc + 4 * u4 + 2]) * inv_l,
+                              __uint_as_float(v[32 * cc + 4 * u4 + 3]) * inv_l);
+          }
+        } else {
+          uint8_t* dst = stage + row * 128;
 #pragma unroll
-            for (int hh = 0; hh < 2; ++hh) {
-              uint32_t rr[32];
-              tmem_ld32(t_o + chunk * 64 + hh * 32, rr);
-              tmem_ld_wait();
+          for (int u4 = 0; u4 < 8; ++u4) {
+            uint32_t wv[4];
 #pragma unroll
-              for (int u4 = 0; u4 < 4; ++u4) {
-                uint32_t wv[4];
-#pragma unroll
-                for (int q2 = 0; q2 < 4; ++q2)
-                  wv[q2] = pack_bf16x2(__uint_as_float(rr[8 * u4 + 2 * q2]) * inv_l,
-                                       __uint_as_float(rr[8 * u4 + 2 * q2 + 1]) * inv_l);
-                *reinterpret_cast<uint4*>(dst + (((hh * 4 + u4) ^ sw) << 4)) =
-                    make_uint4(wv[0], wv[1], wv[2], wv[3]);
-              }
-            }
+            for (int q2 = 0; q2 < 4; ++q2)
+              wv[q2] = pack_bf16x2(__uint_as_float(v[8 * u4 + 2 * q2]) * inv_l,
+                                   __uint_as_float(v[8 * u4 + 2 * q2 + 1]) * inv_l);
+            *reinterpret_cast<uint4*>(dst + ((u4 ^ sw) << 4)) =
+                make_uint4(wv[0], wv[1], wv[2], wv[3]);
           }
         }
         fence_proxy_async_smem();  // the generic-proxy writes become visible to TMA
@@ -737,7 +820,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(
         if (wg_leader) {
           ok = mbar_wait(&bar_stw[t], npass & 1, &abort_flag);
           if (ok) {
-            for (int cc = 0; cc < C::kStageChunks && c0 + cc < n_chunks; ++cc)
+            for (int cc = 0; cc < (f32 ? C::kStageChunks : 1); ++cc)
               tma_store_4d(&tm_o, stage + cc * C::kChunkBytes, (c0 + cc) * (f32 ? 32 : 64),
                            w.kvh * G, pt, w.b);
             bulk_commit_group();
