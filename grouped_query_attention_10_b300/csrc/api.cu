@@ -178,12 +178,14 @@ int prefill_common(const void* q, const void* k, const void* v, const int32_t* k
     const cuuint32_t box[4] = {64, static_cast<cuuint32_t>(G),
                                static_cast<cuuint32_t>(gqa::kPrefillBM / G), 1};
     if (!encode_bf16(&a.tm_q, 4, q, dims, strides, box)) return GQA_ERR_CUDA;
-    // the output has the query layout; boxes are 128-byte column chunks
+    // the output has the query layout; a box is one 128-byte column chunk of
+    // the 32 rows (positions x heads of the group) one warp stores
     const cuuint64_t oe = o_dtype == GQA_OUT_F32 ? 4 : 2;
     const cuuint64_t ostrides[3] = {d * oe, static_cast<cuuint64_t>(h_q) * d * oe,
                                     static_cast<cuuint64_t>(Lq) * h_q * d * oe};
-    const cuuint32_t obox[4] = {static_cast<cuuint32_t>(128 / oe), static_cast<cuuint32_t>(G),
-                                static_cast<cuuint32_t>(gqa::kPrefillBM / G), 1};
+    const cuuint32_t obox[4] = {static_cast<cuuint32_t>(128 / oe),
+                                static_cast<cuuint32_t>(G < 32 ? G : 32),
+                                static_cast<cuuint32_t>(G < 32 ? 32 / G : 1), 1};
     if (!encode_sw128(&a.tm_o, o_dtype == GQA_OUT_F32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32
                                                       : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,
                       4, o, dims, ostrides, obox))

@@ -98,7 +98,9 @@ struct PrefillCfg {
   static constexpr uint32_t kOffV = kOffK + KS * kKVStage;
   // Output staging, per query tile: 128 rows x kStageChunks 128-byte column
   // chunks (a chunk = 32 fp32 or 64 bf16 columns), written by the softmax
-  // threads and stored by TMA (d = 64: the whole tile in one pass).
+  // threads and stored by TMA (d = 64: the whole tile in one pass). Each warp
+  // owns the 32 rows (4 KB of every chunk) of its TMEM lane quadrant and
+  // stores them itself.
   static constexpr int kStageChunks = D == 64 ? 2 : 1;
   static constexpr uint32_t kChunkBytes = BM * 128;
   static constexpr uint32_t kStageBytes = kStageChunks * kChunkBytes;
@@ -224,8 +226,6 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(
   __shared__ __align__(8) uint64_t bar_p2[2];   // d = 128: second half of P_t in TMEM
   __shared__ __align__(8) uint64_t bar_o[2];    // P_t.V retired
   __shared__ __align__(8) uint64_t bar_fin[2];  // every MMA of issuer t retired
-  __shared__ __align__(8) uint64_t bar_stw[2];  // output stage t written (128 arrivals)
-  __shared__ __align__(8) uint64_t bar_stf[2];  // output stage t free again
   __shared__ __align__(8) uint64_t bar_turn[4]; // exponential phases, one per SM sub-partition
   __shared__ uint32_t tmem_base_sh;
   __shared__ int abort_flag;
@@ -260,10 +260,6 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(
     }
     mbar_init(&bar_fin[0], 1);
     mbar_init(&bar_fin[1], 1);
-    mbar_init(&bar_stw[0], 128);
-    mbar_init(&bar_stw[1], 128);
-    mbar_init(&bar_stf[0], 1);
-    mbar_init(&bar_stf[1], 1);
     for (int q = 0; q < 4; ++q) mbar_init(&bar_turn[q], 32);
     fence_mbar_init();
   }
@@ -767,13 +763,14 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(
       // column chunks; rows past L are dropped by the store itself
       const bool f32 = p.o_dtype == GQA_OUT_F32;
       const int n_chunks = f32 ? D / 32 : D / 64;
-      const bool wg_leader = threadIdx.x == 128 + 128 * t;
       uint8_t* stage = smem + C::kOffStage + t * C::kStageBytes;
       const uint32_t sw = static_cast<uint32_t>(row & 7);
-      // staging hand-off through mbarriers (bounded waits): bar_stf[t] phase
-      // k = the stage is free again after pass k, bar_stw[t] phase k = every
-      // thread has written its rows for pass k
-      for (int c0 = 0; c0 < n_chunks && ok; c0 += C::kStageChunks, ++npass) {
+      // this warp's 32 rows start at position pt + (32 wq) / G, head
+      // kvh * G + (32 wq) % G; its TMA store box is 32 rows of the tile
+      const int r0 = wq * 32;
+      const int st_pos = pt + (r0 >> G_log2);
+      const int st_head = w.kvh * G + (r0 & (G - 1));
+      for (int c0 = 0; c0 < n_chunks; c0 += C::kStageChunks, ++npass) {
         // this pass's accumulator columns, read from TMEM before waiting for
         // the stage (fp32: kStageChunks chunks of 32 columns; bf16: one chunk
         // of 64 columns)
@@ -783,12 +780,9 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(
           tmem_ld32(t_o + (f32 ? c0 * 32 + 32 : c0 * 64 + 32), v + 32);
         tmem_ld_wait();
         if (npass > 0) {
-          if (wg_leader) {
-            bulk_wait_read_all();  // the previous pass's stores have read the stage
-            mbar_arrive(&bar_stf[t]);
-          }
-          ok = mbar_wait(&bar_stf[t], (npass - 1) & 1, &abort_flag);
-          if (!ok) break;
+          // the warp's previous stores have read its rows of the stage
+          if (lane == 0) bulk_wait_read_all();
+          __syncwarp();
         }
         if (f32) {
 #pragma unroll
@@ -816,15 +810,15 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(
           }
         }
         fence_proxy_async_smem();  // the generic-proxy writes become visible to TMA
-        mbar_arrive(&bar_stw[t]);
-        if (wg_leader) {
-          ok = mbar_wait(&bar_stw[t], npass & 1, &abort_flag);
-          if (ok) {
+        __syncwarp();
+        if (lane == 0) {
+          // a warp whose rows all lie past the sequence stores nothing
+          if (st_pos < p.Lq) {
             for (int cc = 0; cc < (f32 ? C::kStageChunks : 1); ++cc)
-              tma_store_4d(&tm_o, stage + cc * C::kChunkBytes, (c0 + cc) * (f32 ? 32 : 64),
-                           w.kvh * G, pt, w.b);
-            bulk_commit_group();
+              tma_store_4d(&tm_o, stage + cc * C::kChunkBytes + r0 * 128,
+                           (c0 + cc) * (f32 ? 32 : 64), st_head, st_pos, w.b);
           }
+          bulk_commit_group();
         }
       }
       if (!ok) break;
@@ -833,7 +827,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(
         p.lse[(static_cast<size_t>(w.b) * h_q + head) * p.Lq + pos] =
             l_run > 0.f ? (m_run + __log2f(l_run)) * 0.69314718055994531f : -INFINITY;
     }
-    if (threadIdx.x == 128 + 128 * t) bulk_wait_all();  // output stores complete
+    if (lane == 0) bulk_wait_all();  // this warp's output stores are complete
   }
 
   tc_fence_before();
