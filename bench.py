@@ -49,10 +49,13 @@ NOMINAL_HBM_GBS = 8000.0
 # two roofline kernels, valid only while the kernel sources hash to the
 # prefix given (sha256 over the listed files, concatenated in order).
 PROFILED = {
-    "prefill_causal_d128": {"files": ["prefill.cu", "ptx.cuh"], "sha256_prefix": None,
-                            "dram_bytes": None},
-    "decode_ragged": {"files": ["decode.cu", "ptx.cuh"], "sha256_prefix": None,
-                      "dram_bytes": None},
+    # ncu --set full of one prefill_kernel<128,causal> launch of the causal workload
+    "prefill_causal_d128": {"files": ["prefill.cu", "ptx.cuh"],
+                            "sha256_prefix": "ee8bf52c917b68d5",
+                            "dram_bytes": 436_657_152 + 213_529_856},
+    # ncu --set full of one decode_split_kernel<128,1> launch of the B=64 ragged decode
+    "decode_ragged": {"files": ["decode.cu", "ptx.cuh"], "sha256_prefix": "6caaef4ac65c6a5f",
+                      "dram_bytes": 1_139_231_000 + 11_645_184},
 }
 
 
@@ -63,6 +66,9 @@ def parse_args(argv=None):
     p.add_argument("--warmup", type=int, default=5)
     p.add_argument("--impl", choices=["native", "reference"], default="native")
     p.add_argument("--no-extra", action="store_true", help="skip the context measurements")
+    p.add_argument("--step-only", action="store_true",
+                   help="time the step and print its line without the decode roofline, e2e, "
+                        "CPU and context legs (for launch lists under a profiler)")
     return p.parse_args(argv)
 
 
@@ -489,11 +495,12 @@ def native_arm(args):
     del o_eager, od_eager
     torch.cuda.empty_cache()
 
-    roofline["decode"] = decode_roofline(dev, stream, peaks, peak_src, flush)
-    torch.cuda.empty_cache()
-
-    e2e = e2e_pipelined(args, dev, w, kc, vc, lens, ws, status, flops_step)
-    torch.cuda.empty_cache()
+    e2e = None
+    if not args.step_only:
+        roofline["decode"] = decode_roofline(dev, stream, peaks, peak_src, flush)
+        torch.cuda.empty_cache()
+        e2e = e2e_pipelined(args, dev, w, kc, vc, lens, ws, status, flops_step)
+        torch.cuda.empty_cache()
 
     result = {
         "metric": METRIC,
@@ -524,7 +531,7 @@ def native_arm(args):
         "clocks": clk.summary(),
     }
 
-    if rank == 0 and world == 1:
+    if rank == 0 and world == 1 and not args.step_only:
         budget = float(os.environ.get("GQA_BENCH_CPU_BUDGET_S", "12"))
         tf, groups, dt = cpu_oracle_prefill_sample(budget)
         gbs, nseq, dtd = cpu_oracle_decode_sample(budget / 2)
@@ -537,7 +544,7 @@ def native_arm(args):
                        "sample": f"fp64 NumPy oracle decode of {nseq} ragged sequences "
                                  f"of the decode workload ({dtd:.1f} s)"},
         }
-    if not args.no_extra:
+    if not (args.no_extra or args.step_only):
         result["extra"] = extra_measurements(dev, stream, peaks, peak_src, flush)
     if rank == 0:
         print(json.dumps(result), flush=True)
