@@ -371,6 +371,16 @@ int decode_common(const void* q, const void* k_cache, const void* v_cache,
   a.S_max = S_max;
   a.split_len = lay.split_len;
   a.n_split = lay.n_split;
+  if (window > 0) {
+    // a window's rows are spread over the same n_split splits (and workspace
+    // slots) as a full cache: split length = ceil((W' + 63) / n_split) rounded
+    // up to a 64-row stage, W' = min(W, S_max); the 63 covers the window's
+    // first row sitting anywhere inside its stage
+    const long long w = window < S_max ? window : S_max;
+    long long l = (w + gqa::kDecodeStage - 1 + lay.n_split - 1) / lay.n_split;
+    l = (l + gqa::kDecodeStage - 1) / gqa::kDecodeStage * gqa::kDecodeStage;
+    a.split_len = static_cast<int>(l);
+  }
   a.scale_log2 = scale * 1.4426950408889634f;
   a.window = window;
   a.alibi = alibi_slopes;

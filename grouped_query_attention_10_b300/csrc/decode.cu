@@ -94,12 +94,14 @@ __device__ __forceinline__ Item decode_item(int u, const int32_t* seq_lens, int 
   int len = seq_lens[it.b];
   len = len < 0 ? 0 : (len > S_max ? S_max : len);
   it.len = len;
-  // rows before the sliding window's 64-row stage are not read at all; the
-  // stage start stays a multiple of 64 (of the split length too), so a paged
-  // stage never begins inside a page, and the rows in [s0, lo) are masked
+  // With a sliding window only its rows are read: the splits tile the
+  // window from the 64-row stage that holds its first row (a window of W
+  // rows is spread over all n_split splits, whatever the cache size), and
+  // the rows of that stage before the window are masked. Every stage start
+  // stays a multiple of 64, so a paged stage never begins inside a page.
   it.lo = window > 0 ? max(0, len - window) : 0;
-  it.s0 = max(it.split * split_len, it.lo & ~(kDecodeStage - 1));
-  it.s1 = min(len, it.split * split_len + split_len);
+  it.s0 = (it.lo & ~(kDecodeStage - 1)) + it.split * split_len;
+  it.s1 = min(len, it.s0 + split_len);
   it.n_st = it.s0 < it.s1 ? (it.s1 - it.s0 + kDecodeStage - 1) / kDecodeStage : 0;
   return it;
 }
@@ -484,11 +486,12 @@ __global__ void __launch_bounds__(kCombineThreads) decode_combine_kernel(
   }
   // partials of this row: n_slices per split (one per token slice; a slice
   // that saw no token holds lse = -inf and weighs nothing)
-  // splits wholly before the sliding window were never written
-  const int first = (window > 0 ? max(0, len - window) : 0) / split_len * n_slices;
-  const int n = (len + split_len - 1) / split_len * n_slices - first;
+  // the splits that saw rows (with a window they start at the window's first
+  // 64-row stage); later splits were never written
+  const int base = (window > 0 ? max(0, len - window) : 0) & ~(kDecodeStage - 1);
+  const int n = (len - base + split_len - 1) / split_len * n_slices;
   const int n_part = n_split * n_slices;
-  const float* pl = part_lse + static_cast<size_t>(bh) * n_part + first;
+  const float* pl = part_lse + static_cast<size_t>(bh) * n_part;
   const bool staged = n <= kCombineSmem;
   auto lse_at = [&](int s) { return staged ? wsh[s] : pl[s]; };
   // block max of the partial log-sum-exps
@@ -523,7 +526,7 @@ __global__ void __launch_bounds__(kCombineThreads) decode_combine_kernel(
   // weighted sum of the partial outputs
   const int grp = tid / kLanesPerRow;
   const int c4 = (tid % kLanesPerRow) * 4;
-  const float* po = part_o + (static_cast<size_t>(bh) * n_part + first) * D + c4;
+  const float* po = part_o + static_cast<size_t>(bh) * n_part * D + c4;
   float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll 4
   for (int s = grp; s < n; s += kGroups) {
