@@ -11,22 +11,36 @@
 
 namespace gqa {
 
+// Splits a flat chunk index of the [B, T, g, chunks] new-token layout into
+// (b, t, h, c). Idx is 32-bit when the whole range fits (two 32-bit divisions
+// per chunk, instead of 64-bit ones that made the copy instruction bound).
+template <typename Idx>
+__device__ __forceinline__ void split_chunk(Idx idx, int T, int g, int chunk_log2, int& b, int& t,
+                                            int& h, int& c) {
+  const Idx per_tok = static_cast<Idx>(g) << chunk_log2;  // chunks of one token (all heads)
+  const Idx tok = idx / per_tok;
+  const int i = static_cast<int>(idx - tok * per_tok);
+  h = i >> chunk_log2;
+  c = i & ((1 << chunk_log2) - 1);
+  const Idx bb = tok / static_cast<Idx>(T);
+  b = static_cast<int>(bb);
+  t = static_cast<int>(tok - bb * static_cast<Idx>(T));
+}
+
 // One thread per 16-byte chunk of one (b, t, kv head) row of K and of V.
 // Reads of k_new/v_new are fully coalesced; writes are contiguous per row.
+template <typename Idx>
 __global__ void __launch_bounds__(256) kv_append_rows_kernel(
     uint4* __restrict__ k_cache, uint4* __restrict__ v_cache,
     const int32_t* __restrict__ seq_lens, const uint4* __restrict__ k_new,
-    const uint4* __restrict__ v_new, int B, int g, int chunks, int S_max, int T,
+    const uint4* __restrict__ v_new, int B, int g, int chunk_log2, int S_max, int T,
     int32_t* status) {
-  const long long total = static_cast<long long>(B) * T * g * chunks;
-  for (long long idx = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x; idx < total;
-       idx += static_cast<long long>(gridDim.x) * blockDim.x) {
-    const int c = static_cast<int>(idx % chunks);
-    long long r = idx / chunks;
-    const int h = static_cast<int>(r % g);
-    r /= g;
-    const int t = static_cast<int>(r % T);
-    const int b = static_cast<int>(r / T);
+  const int chunks = 1 << chunk_log2;
+  const Idx total = static_cast<Idx>(B) * T * g * chunks;
+  for (Idx idx = static_cast<Idx>(blockIdx.x) * blockDim.x + threadIdx.x; idx < total;
+       idx += static_cast<Idx>(gridDim.x) * blockDim.x) {
+    int b, t, h, c;
+    split_chunk<Idx>(idx, T, g, chunk_log2, b, t, h, c);
     const int len = seq_lens[b];
     if (len < 0 || len > S_max) {
       if (t == 0 && h == 0 && c == 0) record_status(status, GQA_ERR_BAD_LENGTH);
@@ -58,21 +72,19 @@ __global__ void kv_append_lens_kernel(int32_t* seq_lens, int B, int S_max, int T
 
 // Paged cache: row pos of sequence b lives in row pos % page_size of page
 // block_table[b][pos / page_size] of a [num_pages, g, page_size, d] pool.
+template <typename Idx>
 __global__ void __launch_bounds__(256) kv_append_paged_rows_kernel(
     uint4* __restrict__ k_pool, uint4* __restrict__ v_pool, const int32_t* __restrict__ table,
     const int32_t* __restrict__ seq_lens, const uint4* __restrict__ k_new,
-    const uint4* __restrict__ v_new, int B, int g, int chunks, int page_log2, int num_pages,
+    const uint4* __restrict__ v_new, int B, int g, int chunk_log2, int page_log2, int num_pages,
     int max_blocks, int T, int32_t* status) {
-  const long long total = static_cast<long long>(B) * T * g * chunks;
+  const int chunks = 1 << chunk_log2;
+  const Idx total = static_cast<Idx>(B) * T * g * chunks;
   const int cap = max_blocks << page_log2;
-  for (long long idx = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x; idx < total;
-       idx += static_cast<long long>(gridDim.x) * blockDim.x) {
-    const int c = static_cast<int>(idx % chunks);
-    long long r = idx / chunks;
-    const int h = static_cast<int>(r % g);
-    r /= g;
-    const int t = static_cast<int>(r % T);
-    const int b = static_cast<int>(r / T);
+  for (Idx idx = static_cast<Idx>(blockIdx.x) * blockDim.x + threadIdx.x; idx < total;
+       idx += static_cast<Idx>(gridDim.x) * blockDim.x) {
+    int b, t, h, c;
+    split_chunk<Idx>(idx, T, g, chunk_log2, b, t, h, c);
     const int len = seq_lens[b];
     if (len < 0 || len > cap) {
       if (t == 0 && h == 0 && c == 0) record_status(status, GQA_ERR_BAD_LENGTH);
@@ -99,15 +111,21 @@ cudaError_t launch_append_paged(void* k_pool, void* v_pool, const int32_t* block
                                 int32_t* seq_lens, const void* k_new, const void* v_new, int B,
                                 int g, int d, int page_log2, int num_pages, int max_blocks, int T,
                                 int32_t* status, cudaStream_t s) {
-  const int chunks = d / 8;
-  const long long total = static_cast<long long>(B) * T * g * chunks;
+  const int chunk_log2 = d == 64 ? 3 : 4;  // 16-byte chunks per row: 8 or 16
+  const long long total = static_cast<long long>(B) * T * g << chunk_log2;
   long long blocks = (total + 255) / 256;
   if (blocks > 148LL * 32) blocks = 148LL * 32;
   if (blocks < 1) blocks = 1;
-  kv_append_paged_rows_kernel<<<static_cast<unsigned>(blocks), 256, 0, s>>>(
-      static_cast<uint4*>(k_pool), static_cast<uint4*>(v_pool), block_table, seq_lens,
-      static_cast<const uint4*>(k_new), static_cast<const uint4*>(v_new), B, g, chunks, page_log2,
-      num_pages, max_blocks, T, status);
+  if (total + 148LL * 32 * 256 < (1LL << 31))
+    kv_append_paged_rows_kernel<uint32_t><<<static_cast<unsigned>(blocks), 256, 0, s>>>(
+        static_cast<uint4*>(k_pool), static_cast<uint4*>(v_pool), block_table, seq_lens,
+        static_cast<const uint4*>(k_new), static_cast<const uint4*>(v_new), B, g, chunk_log2,
+        page_log2, num_pages, max_blocks, T, status);
+  else
+    kv_append_paged_rows_kernel<uint64_t><<<static_cast<unsigned>(blocks), 256, 0, s>>>(
+        static_cast<uint4*>(k_pool), static_cast<uint4*>(v_pool), block_table, seq_lens,
+        static_cast<const uint4*>(k_new), static_cast<const uint4*>(v_new), B, g, chunk_log2,
+        page_log2, num_pages, max_blocks, T, status);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   kv_append_lens_kernel<<<(B + 127) / 128, 128, 0, s>>>(seq_lens, B, max_blocks << page_log2, T);
@@ -143,31 +161,34 @@ __device__ __forceinline__ uint32_t pack_bf16_rn(float lo, float hi) {
   return *reinterpret_cast<const uint32_t*>(&v);
 }
 
-template <bool PAGED>
+// Idx: 32-bit when the whole index range fits (cheap divisions), else 64-bit.
+template <bool PAGED, typename Idx>
 __global__ void __launch_bounds__(256) kv_append_rope_kernel(const RopeAppendArgs a) {
-  const int half = a.d / 16;   // threads per row
+  const int half_log2 = a.d == 64 ? 2 : 3;  // threads per row: d / 16
+  const int half = 1 << half_log2;
   const int chunks = a.d / 8;  // 16-byte chunks per row
   const int rows_bt = a.h_q + 2 * a.g;  // query, key and value rows of one token
-  const long long total = static_cast<long long>(a.B) * a.T * rows_bt * half;
+  const Idx total = static_cast<Idx>(a.B) * a.T * rows_bt * half;
   const int cap = PAGED ? (a.max_blocks << a.page_log2) : a.S_max;
   const int lane = threadIdx.x & 31;
-  const long long stride = static_cast<long long>(gridDim.x) * blockDim.x;
+  const Idx stride = static_cast<Idx>(gridDim.x) * blockDim.x;
   const float4* cos4 = reinterpret_cast<const float4*>(a.cos);
   const float4* sin4 = reinterpret_cast<const float4*>(a.sin);
-  for (long long base = static_cast<long long>(blockIdx.x) * blockDim.x + (threadIdx.x & ~31);
-       base < total; base += stride) {
-    const long long idx = base + lane;
+  for (Idx base = static_cast<Idx>(blockIdx.x) * blockDim.x + (threadIdx.x & ~31); base < total;
+       base += stride) {
+    const Idx idx = base + lane;
     bool act = idx < total;
     uint4 out0 = make_uint4(0u, 0u, 0u, 0u), out1 = out0;
     uint4* dst0 = nullptr;
     uint4* dst1 = nullptr;
     if (act) {
-      const int u = static_cast<int>(idx % half);
-      const long long r = idx / half;
-      const int row = static_cast<int>(r % rows_bt);
-      const long long bt = r / rows_bt;
-      const int t = static_cast<int>(bt % a.T);
-      const int b = static_cast<int>(bt / a.T);
+      const int u = static_cast<int>(idx & (half - 1));
+      const Idx r = idx >> half_log2;
+      const Idx bt = r / static_cast<Idx>(rows_bt);
+      const int row = static_cast<int>(r - bt * static_cast<Idx>(rows_bt));
+      const Idx bq = bt / static_cast<Idx>(a.T);
+      const int t = static_cast<int>(bt - bq * static_cast<Idx>(a.T));
+      const int b = static_cast<int>(bq);
       const int len = a.seq_lens[b];
       int pos = 0;
       if (len < 0 || len > cap) {
@@ -251,10 +272,15 @@ cudaError_t launch_append_rope(const RopeAppendArgs& a, cudaStream_t s) {
   if (blocks > 148LL * 16) blocks = 148LL * 16;  // grid-stride beyond 16 CTAs per SM
   if (blocks < 1) blocks = 1;
   const bool paged = a.table != nullptr;
-  if (paged)
-    kv_append_rope_kernel<true><<<static_cast<unsigned>(blocks), 256, 0, s>>>(a);
+  const bool narrow = total + 148LL * 16 * 256 < (1LL << 31);
+  if (paged && narrow)
+    kv_append_rope_kernel<true, uint32_t><<<static_cast<unsigned>(blocks), 256, 0, s>>>(a);
+  else if (paged)
+    kv_append_rope_kernel<true, uint64_t><<<static_cast<unsigned>(blocks), 256, 0, s>>>(a);
+  else if (narrow)
+    kv_append_rope_kernel<false, uint32_t><<<static_cast<unsigned>(blocks), 256, 0, s>>>(a);
   else
-    kv_append_rope_kernel<false><<<static_cast<unsigned>(blocks), 256, 0, s>>>(a);
+    kv_append_rope_kernel<false, uint64_t><<<static_cast<unsigned>(blocks), 256, 0, s>>>(a);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   const int cap = paged ? (a.max_blocks << a.page_log2) : a.S_max;
@@ -265,15 +291,22 @@ cudaError_t launch_append_rope(const RopeAppendArgs& a, cudaStream_t s) {
 cudaError_t launch_append(void* k_cache, void* v_cache, int32_t* seq_lens, const void* k_new,
                           const void* v_new, int B, int g, int d, int S_max, int T,
                           int32_t* status, cudaStream_t s) {
-  const int chunks = d / 8;
-  const long long total = static_cast<long long>(B) * T * g * chunks;
+  const int chunk_log2 = d == 64 ? 3 : 4;  // 16-byte chunks per row: 8 or 16
+  const long long total = static_cast<long long>(B) * T * g << chunk_log2;
   long long blocks = (total + 255) / 256;
   if (blocks > 148LL * 32) blocks = 148LL * 32;  // grid-stride beyond 32 CTAs per SM
   if (blocks < 1) blocks = 1;
-  kv_append_rows_kernel<<<static_cast<unsigned>(blocks), 256, 0, s>>>(
-      static_cast<uint4*>(k_cache), static_cast<uint4*>(v_cache), seq_lens,
-      static_cast<const uint4*>(k_new), static_cast<const uint4*>(v_new), B, g, chunks, S_max, T,
-      status);
+  // 32-bit indices whenever the range (plus one grid stride) fits
+  if (total + 148LL * 32 * 256 < (1LL << 31))
+    kv_append_rows_kernel<uint32_t><<<static_cast<unsigned>(blocks), 256, 0, s>>>(
+        static_cast<uint4*>(k_cache), static_cast<uint4*>(v_cache), seq_lens,
+        static_cast<const uint4*>(k_new), static_cast<const uint4*>(v_new), B, g, chunk_log2,
+        S_max, T, status);
+  else
+    kv_append_rows_kernel<uint64_t><<<static_cast<unsigned>(blocks), 256, 0, s>>>(
+        static_cast<uint4*>(k_cache), static_cast<uint4*>(v_cache), seq_lens,
+        static_cast<const uint4*>(k_new), static_cast<const uint4*>(v_new), B, g, chunk_log2,
+        S_max, T, status);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   kv_append_lens_kernel<<<(B + 127) / 128, 128, 0, s>>>(seq_lens, B, S_max, T);

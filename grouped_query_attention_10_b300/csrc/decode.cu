@@ -15,7 +15,8 @@
 //    MMAs, so each K/V byte is read from HBM once per K/V head, never once
 //    per query head. Every item ends with its normalised partial output and
 //    its log2 sum-exp.
-//  * pass 2 (decode_combine_kernel): log-sum-exp combine of the partials.
+//  * pass 2 (decode_combine_kernel): log-sum-exp combine of the partials,
+//    launched as a programmatic dependent of pass 1.
 #include <cuda_bf16.h>
 
 #include "../../include/gqa.h"
@@ -454,6 +455,9 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) decode_split_kernel(
   }
   __syncthreads();
   if (tid == 0 && abort_flag) record_status(status, GQA_ERR_TIMEOUT);
+  // the combine (launched as a programmatic dependent) may start launching;
+  // it waits for this whole grid before it reads a partial
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }
 
 // One CTA per (sequence, query head): merge the partials that hold data.
@@ -476,6 +480,9 @@ __global__ void __launch_bounds__(kCombineThreads) decode_combine_kernel(
   __shared__ float red[kWarps];
   __shared__ float wsh[kCombineSmem];
   __shared__ float acc_sh[kGroups][D];
+  // launched as a programmatic dependent of the split pass: wait until that
+  // grid has completed and its partials are visible
+  asm volatile("griddepcontrol.wait;" ::: "memory");
   const int bh = blockIdx.x;
   const int b = bh / h_q;
   const int tid = threadIdx.x;
@@ -602,11 +609,23 @@ static cudaError_t launch_decode_t(const DecodeArgs& a, cudaStream_t s) {
       a.item_counter, a.status);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  decode_combine_kernel<D><<<a.B * a.h_q, kCombineThreads, 0, s>>>(a.part_o, a.part_lse, a.seq_lens, a.o,
-                                                      a.o_dtype, a.lse, a.h_q, a.S_max,
-                                                      a.split_len, a.n_split, kConsumers / MT,
-                                                      a.window, a.status);
-  return cudaGetLastError();
+  // The combine is a programmatic dependent launch: its CTAs are scheduled
+  // while the split pass drains and block in griddepcontrol.wait until it
+  // has finished, which hides most of the launch gap between the two.
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(a.B * a.h_q));
+  cfg.blockDim = dim3(kCombineThreads);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, decode_combine_kernel<D>, static_cast<const float*>(a.part_o),
+                            static_cast<const float*>(a.part_lse), a.seq_lens, a.o, a.o_dtype,
+                            a.lse, a.h_q, a.S_max, a.split_len, a.n_split, kConsumers / MT,
+                            a.window, a.status);
 }
 
 cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t s) {
