@@ -279,6 +279,10 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(
       prefetch_tmap(&tm_q);
       prefetch_tmap(&tm_k);
       prefetch_tmap(&tm_v);
+      // K/V tiles are re-read by the other units of their (batch, K/V head)
+      // pair: keep them in L2; each query tile is read once: stream it
+      const uint64_t keep = l2_policy_evict_last();
+      const uint64_t stream = l2_policy_evict_first();
       int nu = 0, kc = 0, vc = 0;  // units, K tiles and V tiles issued so far
       bool ok = true;
       for (int u = blockIdx.x; u < n_units && ok; u += gridDim.x, ++nu) {
@@ -292,8 +296,8 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(
         for (int t = 0; t < n_qt; ++t) {
 #pragma unroll
           for (int cb = 0; cb < D / 64; ++cb)
-            tma_load_4d(smem + qs * C::kQSlot + t * C::kQTile + cb * (BM * 128), &tm_q,
-                        &bar_q[qs], cb * 64, w.kvh * G, w.p0 + t * PM, w.b);
+            tma_load_4d_hint(smem + qs * C::kQSlot + t * C::kQTile + cb * (BM * 128), &tm_q,
+                             &bar_q[qs], cb * 64, w.kvh * G, w.p0 + t * PM, w.b, stream);
         }
         for (int j = 0; j < n_kv && ok; ++j) {
           const int ks = kc % KS;
@@ -304,9 +308,11 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(
           for (int cb = 0; cb < D / 64; ++cb) {
             uint8_t* dst = smem + C::kOffK + ks * C::kKVStage + cb * (BN * 128);
             if (kCache)  // 3-D map over the cache
-              tma_load_3d(dst, &tm_k, &bar_kf[ks], cb * 64, (w.kv0 + j) * BN, w.b * g + w.kvh);
+              tma_load_3d_hint(dst, &tm_k, &bar_kf[ks], cb * 64, (w.kv0 + j) * BN,
+                               w.b * g + w.kvh, keep);
             else
-              tma_load_4d(dst, &tm_k, &bar_kf[ks], cb * 64, w.kvh, (w.kv0 + j) * BN, w.b);
+              tma_load_4d_hint(dst, &tm_k, &bar_kf[ks], cb * 64, w.kvh, (w.kv0 + j) * BN, w.b,
+                               keep);
           }
           ++kc;
           const int vs = vc % VS;
@@ -317,9 +323,11 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(
           for (int cb = 0; cb < D / 64; ++cb) {
             uint8_t* dst = smem + C::kOffV + vs * C::kKVStage + cb * (BN * 128);
             if (kCache)  // 3-D map over the cache
-              tma_load_3d(dst, &tm_v, &bar_vf[vs], cb * 64, (w.kv0 + j) * BN, w.b * g + w.kvh);
+              tma_load_3d_hint(dst, &tm_v, &bar_vf[vs], cb * 64, (w.kv0 + j) * BN,
+                               w.b * g + w.kvh, keep);
             else
-              tma_load_4d(dst, &tm_v, &bar_vf[vs], cb * 64, w.kvh, (w.kv0 + j) * BN, w.b);
+              tma_load_4d_hint(dst, &tm_v, &bar_vf[vs], cb * 64, w.kvh, (w.kv0 + j) * BN, w.b,
+                               keep);
           }
           ++vc;
         }
@@ -549,6 +557,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(
     const uint32_t t_p = tmem + lane_base + C::kColP + static_cast<uint32_t>(t) * C::kStrideP;
     const float scale_log2 = p.scale_log2;
     const uint64_t c2 = f32x2(scale_log2, scale_log2);
+    const uint64_t o_policy = l2_policy_evict_first();  // O is written once: stream it
     int it = 0;      // (unit, K/V tile) steps of this query tile so far
     int npass = 0;   // output staging passes of this query tile so far
     int kturn = 0;   // exponential phases of both tiles in earlier units
@@ -815,8 +824,8 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(
           // a warp whose rows all lie past the sequence stores nothing
           if (st_pos < p.Lq) {
             for (int cc = 0; cc < (f32 ? C::kStageChunks : 1); ++cc)
-              tma_store_4d(&tm_o, stage + cc * C::kChunkBytes + r0 * 128,
-                           (c0 + cc) * (f32 ? 32 : 64), st_head, st_pos, w.b);
+              tma_store_4d_hint(&tm_o, stage + cc * C::kChunkBytes + r0 * 128,
+                                (c0 + cc) * (f32 ? 32 : 64), st_head, st_pos, w.b, o_policy);
           }
           bulk_commit_group();
         }
