@@ -51,8 +51,8 @@ NOMINAL_HBM_GBS = 8000.0
 PROFILED = {
     # ncu --set full of one prefill_kernel<128,causal> launch of the causal workload
     "prefill_causal_d128": {"files": ["prefill.cu", "ptx.cuh"],
-                            "sha256_prefix": "ee8bf52c917b68d5",
-                            "dram_bytes": 436_657_152 + 213_529_856},
+                            "sha256_prefix": "3a3f15a847eac988",
+                            "dram_bytes": 363_880_960 + 207_584_768},
     # ncu --set full of one decode_split_kernel<128,1> launch of the B=64 ragged decode
     "decode_ragged": {"files": ["decode.cu", "ptx.cuh"], "sha256_prefix": "70827cfece5998b3",
                       "dram_bytes": 1_139_270_000 + 11_766_528},
@@ -563,10 +563,29 @@ def decode_roofline(dev, stream, peaks, peak_src, flush, n_calls=60):
     o = torch.empty((w.B, w.h_q, w.d), dtype=torch.float32, device=dev)
     ws = torch.empty(gqa.gqa_decode_workspace_bytes(w.B, w.h_q, w.g, w.d, w.S_max),
                      dtype=torch.uint8, device=dev)
-    fn = lambda: gqa.gqa_decode_fwd(q, kc, vc, lens, scale=w.scale, out=o, workspace=ws,
-                                    stream=stream)
+    eager = lambda s_: gqa.gqa_decode_fwd(q, kc, vc, lens, scale=w.scale, out=o, workspace=ws,
+                                          stream=s_)
+    eager(stream)
+    torch.cuda.synchronize()
+    o_eager = o.clone()
+    # timed as a CUDA graph of the library call (counter reset, split pass,
+    # combine), as a serving loop replays it; the replay must match the eager
+    # call bit for bit
+    cap = torch.cuda.Stream(dev)
+    cap.wait_stream(stream)
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(cap):
+        with torch.cuda.graph(graph, stream=cap):
+            eager(cap)
+    torch.cuda.synchronize()
+    graph.replay()
+    torch.cuda.synchronize()
+    if not torch.equal(o, o_eager):
+        raise RuntimeError("graph replay of the decode differs from the eager call")
+    fn = graph.replay
     _time_calls(fn, 5, stream, flush)
     ts = _time_calls(fn, n_calls, stream, flush)
+    ts_eager = _time_calls(lambda: eager(stream), 20, stream, flush)
     nbytes = accounting.decode_kv_bytes(lens.tolist(), w.g, w.d)
     t = statistics.mean(ts)
     gbs = nbytes / t / 1e9
@@ -580,7 +599,9 @@ def decode_roofline(dev, stream, peaks, peak_src, flush, n_calls=60):
         "traffic_unit": "bytes per launch of decode_split_kernel (ncu dram read+write)",
         "algorithmic_bytes": nbytes, "launch_us": round(t * 1e6, 2),
         "median_us": round(statistics.median(ts) * 1e6, 2),
-        "timed": f"CUDA events, mean of {n_calls} calls, L2 flushed before each",
+        "eager_us": round(statistics.mean(ts_eager) * 1e6, 2),
+        "timed": f"CUDA events, mean of {n_calls} replays of a CUDA graph of the call "
+                 "(counter reset + split pass + combine), L2 flushed before each",
     }
     return block
 
