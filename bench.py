@@ -693,8 +693,10 @@ def extra_measurements(dev, stream, peaks, peak_src, flush):
     def one(name, n=20, peak=None, nominal=None):
         fn, work, unit, div = run_workload.make(name, dev)
         call = lambda: fn(stream)
-        _time_calls(call, 3, stream, flush)
-        ts = _time_calls(call, n, stream, flush)
+        reset = getattr(fn, "reset", None)  # an append's empty-cache reset, untimed
+        prep = flush if reset is None else (lambda: (reset(), flush()))
+        _time_calls(call, 3, stream, prep)
+        ts = _time_calls(call, n, stream, prep)
         t = statistics.mean(ts)
         rate = work / t / div
         rec = {"rate": round(rate, 2), "unit": unit, "us": round(t * 1e6, 2)}

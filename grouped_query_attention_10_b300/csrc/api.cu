@@ -372,13 +372,19 @@ int decode_common(const void* q, const void* k_cache, const void* v_cache,
   a.split_len = lay.split_len;
   a.n_split = lay.n_split;
   if (window > 0) {
-    // a window's rows are spread over the same n_split splits (and workspace
-    // slots) as a full cache: split length = ceil((W' + 63) / n_split) rounded
-    // up to a 64-row stage, W' = min(W, S_max); the 63 covers the window's
-    // first row sitting anywhere inside its stage
+    // A window reads at most W' + 63 rows per sequence (W' = min(W, S_max);
+    // the 63 covers its first row sitting anywhere inside a 64-row stage).
+    // The split length follows the same rule as for a cache of that many
+    // rows, so a short window is not cut into needlessly small items; if that
+    // needed more splits than the workspace holds, the window's rows are
+    // spread over the workspace's n_split splits instead.
     const long long w = window < S_max ? window : S_max;
-    long long l = (w + gqa::kDecodeStage - 1 + lay.n_split - 1) / lay.n_split;
-    l = (l + gqa::kDecodeStage - 1) / gqa::kDecodeStage * gqa::kDecodeStage;
+    const long long rows = w + gqa::kDecodeStage - 1;
+    long long l = gqa::decode_split_len(B, h_q, g, static_cast<int>(rows));
+    if ((rows + l - 1) / l > lay.n_split) {
+      l = (rows + lay.n_split - 1) / lay.n_split;
+      l = (l + gqa::kDecodeStage - 1) / gqa::kDecodeStage * gqa::kDecodeStage;
+    }
     a.split_len = static_cast<int>(l);
   }
   a.scale_log2 = scale * 1.4426950408889634f;

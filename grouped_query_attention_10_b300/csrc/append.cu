@@ -27,6 +27,14 @@ __device__ __forceinline__ void split_chunk(Idx idx, int T, int g, int chunk_log
   t = static_cast<int>(tok - bb * static_cast<Idx>(T));
 }
 
+// End of a row-copy CTA: every length its threads read has been read, so the
+// length update (a programmatic dependent launch) may start once all CTAs
+// have passed this point; it need not wait for the copies to land.
+__device__ __forceinline__ void lengths_read() {
+  __syncthreads();
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // One thread per 16-byte chunk of one (b, t, kv head) row of K and of V.
 // Reads of k_new/v_new are fully coalesced; writes are contiguous per row.
 template <typename Idx>
@@ -57,10 +65,14 @@ __global__ void __launch_bounds__(256) kv_append_rows_kernel(
     k_cache[dst] = k_new[src];
     v_cache[dst] = v_new[src];
   }
+  lengths_read();
 }
 
-// Advance every valid length by T, saturating at S_max. Runs after the row
-// copy (same stream), so no row-copy thread can observe the new length.
+// Advance every valid length by T, saturating at S_max. Launched as a
+// programmatic dependent of the row copy: it starts once every row-copy CTA
+// has read its lengths (lengths_read), so no row-copy thread can observe the
+// new length; the row stores may still be in flight, and the next operation
+// on the stream waits for both kernels as usual.
 __global__ void kv_append_lens_kernel(int32_t* seq_lens, int B, int S_max, int T) {
   const int b = blockIdx.x * blockDim.x + threadIdx.x;
   if (b >= B) return;
@@ -68,6 +80,20 @@ __global__ void kv_append_lens_kernel(int32_t* seq_lens, int B, int S_max, int T
   if (len < 0 || len > S_max) return;  // flagged by the row kernel, left as is
   const long long n = static_cast<long long>(len) + T;
   seq_lens[b] = static_cast<int32_t>(n < S_max ? n : S_max);
+}
+
+static cudaError_t launch_lens_update(int32_t* seq_lens, int B, int cap, int T, cudaStream_t s) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>((B + 127) / 128));
+  cfg.blockDim = dim3(128);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kv_append_lens_kernel, seq_lens, B, cap, T);
 }
 
 // Paged cache: row pos of sequence b lives in row pos % page_size of page
@@ -105,6 +131,7 @@ __global__ void __launch_bounds__(256) kv_append_paged_rows_kernel(
     k_pool[dst] = k_new[idx];
     v_pool[dst] = v_new[idx];
   }
+  lengths_read();
 }
 
 cudaError_t launch_append_paged(void* k_pool, void* v_pool, const int32_t* block_table,
@@ -128,8 +155,7 @@ cudaError_t launch_append_paged(void* k_pool, void* v_pool, const int32_t* block
         page_log2, num_pages, max_blocks, T, status);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  kv_append_lens_kernel<<<(B + 127) / 128, 128, 0, s>>>(seq_lens, B, max_blocks << page_log2, T);
-  return cudaGetLastError();
+  return launch_lens_update(seq_lens, B, max_blocks << page_log2, T, s);
 }
 
 // ---------------------------------------------------------------------------
@@ -264,6 +290,7 @@ __global__ void __launch_bounds__(256) kv_append_rope_kernel(const RopeAppendArg
       *dst1 = out1;
     }
   }
+  lengths_read();
 }
 
 cudaError_t launch_append_rope(const RopeAppendArgs& a, cudaStream_t s) {
@@ -284,8 +311,7 @@ cudaError_t launch_append_rope(const RopeAppendArgs& a, cudaStream_t s) {
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   const int cap = paged ? (a.max_blocks << a.page_log2) : a.S_max;
-  kv_append_lens_kernel<<<(a.B + 127) / 128, 128, 0, s>>>(a.seq_lens, a.B, cap, a.T);
-  return cudaGetLastError();
+  return launch_lens_update(a.seq_lens, a.B, cap, a.T, s);
 }
 
 cudaError_t launch_append(void* k_cache, void* v_cache, int32_t* seq_lens, const void* k_new,
@@ -309,8 +335,7 @@ cudaError_t launch_append(void* k_cache, void* v_cache, int32_t* seq_lens, const
         S_max, T, status);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  kv_append_lens_kernel<<<(B + 127) / 128, 128, 0, s>>>(seq_lens, B, S_max, T);
-  return cudaGetLastError();
+  return launch_lens_update(seq_lens, B, S_max, T, s);
 }
 
 }  // namespace gqa
