@@ -68,11 +68,12 @@ __global__ void __launch_bounds__(256) kv_append_rows_kernel(
   lengths_read();
 }
 
-// Advance every valid length by T, saturating at S_max. Launched as a
-// programmatic dependent of the row copy: it starts once every row-copy CTA
-// has read its lengths (lengths_read), so no row-copy thread can observe the
-// new length; the row stores may still be in flight, and the next operation
-// on the stream waits for both kernels as usual.
+// Advance every valid length by T, saturating at S_max. After the K/V row
+// copies it is launched as a programmatic dependent: it starts once every
+// row-copy CTA has read its lengths (lengths_read), so no row-copy thread can
+// observe the new length; the row stores may still be in flight, and the next
+// operation on the stream waits for both kernels as usual. After the RoPE
+// append it runs in plain stream order.
 __global__ void kv_append_lens_kernel(int32_t* seq_lens, int B, int S_max, int T) {
   const int b = blockIdx.x * blockDim.x + threadIdx.x;
   if (b >= B) return;
@@ -290,7 +291,6 @@ __global__ void __launch_bounds__(256) kv_append_rope_kernel(const RopeAppendArg
       *dst1 = out1;
     }
   }
-  lengths_read();
 }
 
 cudaError_t launch_append_rope(const RopeAppendArgs& a, cudaStream_t s) {
@@ -311,7 +311,10 @@ cudaError_t launch_append_rope(const RopeAppendArgs& a, cudaStream_t s) {
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   const int cap = paged ? (a.max_blocks << a.page_log2) : a.S_max;
-  return launch_lens_update(a.seq_lens, a.B, cap, a.T, s);
+  // stream order here: as a programmatic dependent the update measured ~4 %
+  // slower for this kernel (while it gains ~3 % after the plain row copies)
+  kv_append_lens_kernel<<<(a.B + 127) / 128, 128, 0, s>>>(a.seq_lens, a.B, cap, a.T);
+  return cudaGetLastError();
 }
 
 cudaError_t launch_append(void* k_cache, void* v_cache, int32_t* seq_lens, const void* k_new,
