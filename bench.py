@@ -51,8 +51,8 @@ NOMINAL_HBM_GBS = 8000.0
 PROFILED = {
     # ncu --set full of one prefill_kernel<128,causal> launch of the causal workload
     "prefill_causal_d128": {"files": ["prefill.cu", "ptx.cuh"],
-                            "sha256_prefix": "3a3f15a847eac988",
-                            "dram_bytes": 363_880_960 + 207_584_768},
+                            "sha256_prefix": "3e2c4bf7f9b14d7f",
+                            "dram_bytes": 363_915_264 + 207_840_512},
     # ncu --set full of one decode_split_kernel<128,1> launch of the B=64 ragged decode
     "decode_ragged": {"files": ["decode.cu", "ptx.cuh"], "sha256_prefix": "caeeea7b5ef85a6f",
                       "dram_bytes": 1_139_224_000 + 11_682_304},

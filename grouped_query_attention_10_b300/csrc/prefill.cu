@@ -85,6 +85,16 @@ static_assert(128 * kRegsCtl + 256 * kRegsSoftmax <= kThreads * kRegsLaunch,
               "register plan exceeds the launch pool");
 static_assert(kThreads * kRegsLaunch <= 65536, "launch pool exceeds the register file");
 
+// lo += the bf16 in bits 0..15 of w, hi += the bf16 in bits 16..31: each
+// widened exactly to fp32 and added with one rounding (mixed-precision add of
+// sm_100 and later)
+__device__ __forceinline__ void add_bf16x2_to_f32(uint32_t w, float& lo, float& hi) {
+  asm("{ .reg .b16 l, h; mov.b32 {l, h}, %2; add.rn.f32.bf16 %0, l, %0; "
+      "add.rn.f32.bf16 %1, h, %1; }"
+      : "+f"(lo), "+f"(hi)
+      : "r"(w));
+}
+
 template <int D>
 struct PrefillCfg {
   static constexpr bool kSepP = D == 64;           // P_t has TMEM columns of its own
@@ -229,6 +239,9 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(
   __shared__ __align__(8) uint64_t bar_turn[4]; // exponential phases, one per SM sub-partition
   __shared__ uint32_t tmem_base_sh;
   __shared__ int abort_flag;
+  // ALiBi: the column offsets 0 .. BN-1 as floats, read as packed operands
+  __shared__ __align__(16) float s_cols[kAlibi ? BN : 4];
+  if (kAlibi && threadIdx.x < BN) s_cols[threadIdx.x] = static_cast<float>(threadIdx.x);
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -615,19 +628,33 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(
             // every visible key is at or before the query: the bias of key
             // key0 + e is b0 + slope * e
             const float b0 = -slope_log2 * static_cast<float>(q_abs - key0);
+            // two keys per packed op: t = slope * e + b0, x = s * scale + t
+            // (the same roundings as one fmaf each)
+            const uint64_t sc2 = f32x2(scale_log2, scale_log2);
+            const uint64_t sl2 = f32x2(slope_log2, slope_log2);
+            const uint64_t b02 = f32x2(b0, b0);
+            const float4* cols = reinterpret_cast<const float4*>(s_cols);
+#pragma unroll
+            for (int e4 = 0; e4 < BN / 4; ++e4) {
+              const float4 ev = cols[e4];
+              const uint64_t x0 = ffma_x2(u32x2(r[4 * e4], r[4 * e4 + 1]), sc2,
+                                          ffma_x2(sl2, f32x2(ev.x, ev.y), b02));
+              const uint64_t x1 = ffma_x2(u32x2(r[4 * e4 + 2], r[4 * e4 + 3]), sc2,
+                                          ffma_x2(sl2, f32x2(ev.z, ev.w), b02));
+              float xa, xb, xc, xd;
+              split_f32x2(x0, xa, xb);
+              split_f32x2(x1, xc, xd);
+              r[4 * e4] = __float_as_uint(xa);
+              r[4 * e4 + 1] = __float_as_uint(xb);
+              r[4 * e4 + 2] = __float_as_uint(xc);
+              r[4 * e4 + 3] = __float_as_uint(xd);
+            }
             if (need_mask) {
 #pragma unroll
               for (int e = 0; e < BN; ++e) {
                 const int key = key0 + e;
-                const float x = fmaf(__uint_as_float(r[e]), scale_log2,
-                                     fmaf(slope_log2, static_cast<float>(e), b0));
-                r[e] = __float_as_uint(key > last_key || key < first_key ? -INFINITY : x);
+                if (key > last_key || key < first_key) r[e] = 0xff800000u;  // -inf
               }
-            } else {
-#pragma unroll
-              for (int e = 0; e < BN; ++e)
-                r[e] = __float_as_uint(fmaf(__uint_as_float(r[e]), scale_log2,
-                                            fmaf(slope_log2, static_cast<float>(e), b0)));
             }
           } else {
 #pragma unroll
@@ -720,6 +747,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(
         const uint64_t nm2 = f32x2(-m_use, -m_use);
         const uint64_t one2 = f32x2(1.f, 1.f);
         uint64_t sum2[2] = {0ull, 0ull};
+        float bsum[4] = {0.f, 0.f, 0.f, 0.f};  // ALiBi: sums of the bf16 weights, four chains
 #pragma unroll
         for (int hh = 0; hh < 2; ++hh) {
           uint32_t pw[32];
@@ -735,7 +763,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(
               // ALiBi makes rows peaked (one weight near 1): sum the bf16
               // weights the P.V product really uses, so numerator and
               // denominator round alike
-              sum2[e & 1] = fadd_x2(sum2[e & 1], u32x2(pw[e] << 16, pw[e] & 0xffff0000u));
+              add_bf16x2_to_f32(pw[e], bsum[(e & 1) * 2], bsum[(e & 1) * 2 + 1]);
             } else {
               sum2[e & 1] = fadd_x2(sum2[e & 1], f32x2(pa, pb));
             }
@@ -753,6 +781,10 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(
         tmem_st_wait();
         tc_fence_before();
         mbar_arrive(kSepP ? &bar_p[t] : &bar_p2[t]);
+        if (kAlibi) {
+          sum2[0] = f32x2(bsum[0], bsum[1]);
+          sum2[1] = f32x2(bsum[2], bsum[3]);
+        }
         float a0, a1, b0, b1;
         split_f32x2(sum2[0], a0, a1);
         split_f32x2(sum2[1], b0, b1);
