@@ -259,6 +259,64 @@ def test_decode_window_alibi(G_cfg, window, alibi):
     assert_close(f64(lse), lse_ref, "lse")
 
 
+@pytest.mark.parametrize("alibi", [False, True])
+def test_decode_window_split_from_the_window(alibi):
+    # 30 sequences x 8 K/V heads fill the CTA slots with one split per
+    # segment, so a 256-row window is read as one item per segment while the
+    # 4096-row cache (more than one longest item) is split in two. Rows before
+    # the window hold NaN and must never be read.
+    B, h_q, g, d, S_max, W = 30, 32, 8, 64, 4096, 256
+    kc = rand_bf16((B, g, S_max, d), 1201)
+    vc = rand_bf16((B, g, S_max, d), 1202)
+    q = rand_bf16((B, h_q, d), 1203)
+    gen = torch.Generator().manual_seed(1204)
+    lens_l = torch.randint(2100, S_max + 1, (B,), generator=gen).tolist()
+    lens_l[0], lens_l[1] = S_max, W - 3  # a full cache and one shorter than the window
+    for b, n in enumerate(lens_l):
+        lo = max(0, n - W)
+        kc[b, :, :lo] = float("nan")
+        vc[b, :, :lo] = float("nan")
+    slopes = alibi_slopes(h_q) if alibi else None
+    status = torch.zeros(1, dtype=torch.int32, device=DEV)
+    go = guard.empty((B, h_q, d), torch.float32, DEV)
+    o = gqa.gqa_decode_fwd(q, kc, vc, torch.tensor(lens_l, dtype=torch.int32, device=DEV),
+                           scale=0.125, window=W, alibi_slopes=slopes, status=status,
+                           out=go.tensor)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    go.assert_bands("window-split decode O")
+    # the oracle reads only the window: its rows moved to the front of a
+    # compact cache (ALiBi depends on relative positions only)
+    n_w = [min(W, n) for n in lens_l]
+    kw = np.zeros((B, g, W, d))
+    vw = np.zeros((B, g, W, d))
+    for b, n in enumerate(lens_l):
+        kw[b, :, :n_w[b]] = f64(kc[b, :, n - n_w[b]:n])
+        vw[b, :, :n_w[b]] = f64(vc[b, :, n - n_w[b]:n])
+    sl = None if slopes is None else slopes.cpu().numpy().astype(np.float64)
+    o_ref, _ = oracle.decode(f64(q), kw, vw, n_w, 0.125, alibi_slopes=sl)
+    assert_close(f64(o), o_ref, f"window-split decode alibi={alibi}")
+
+
+def test_decode_window_longer_than_the_cache_with_few_segments():
+    # 4 segments and a window longer than the cache: splitting W' + 63 rows
+    # by the cache rule would need more splits than the workspace holds, so
+    # the window's rows are spread over the workspace's splits
+    h_q, g = 32, 1
+    B, d, S_max = 4, 128, 3000
+    kc = rand_bf16((B, g, S_max, d), 1301)
+    vc = rand_bf16((B, g, S_max, d), 1302)
+    q = rand_bf16((B, h_q, d), 1303)
+    lens_l = [3000, 2999, 64, 1]
+    status = torch.zeros(1, dtype=torch.int32, device=DEV)
+    o = gqa.gqa_decode_fwd(q, kc, vc, torch.tensor(lens_l, dtype=torch.int32, device=DEV),
+                           scale=0.0884, window=5000, status=status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    o_ref, _ = oracle.decode(f64(q), f64(kc), f64(vc), lens_l, 0.0884)
+    assert_close(f64(o), o_ref, "window > cache, few segments")
+
+
 def test_decode_equals_one_token_chunked_prefill_with_bias():
     B, h_q, g, d, S_max = 3, 32, 8, 128, 1500
     kc = rand_bf16((B, g, S_max, d), 1101)
