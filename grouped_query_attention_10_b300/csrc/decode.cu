@@ -65,6 +65,16 @@ __device__ __forceinline__ void mma16816(float* c, const uint32_t* a, uint32_t b
       : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
 }
 
+// lo += the bf16 in bits 0..15 of w, hi += the bf16 in bits 16..31: each
+// widened exactly to fp32 and added with one rounding (mixed-precision add of
+// sm_100 and later)
+__device__ __forceinline__ void add_bf16x2_to_f32(uint32_t w, float& lo, float& hi) {
+  asm("{ .reg .b16 l, h; mov.b32 {l, h}, %2; add.rn.f32.bf16 %0, l, %0; "
+      "add.rn.f32.bf16 %1, h, %1; }"
+      : "+f"(lo), "+f"(hi)
+      : "r"(w));
+}
+
 // Byte offset of 16-byte chunk `chunk` (0..7) of row `row` inside one
 // [rows x 128 B] box written by TMA with the 128-byte swizzle.
 __device__ __forceinline__ uint32_t sw128(int row, int chunk) {
@@ -124,6 +134,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) decode_split_kernel(
   constexpr int kCB = C::kCB;
   constexpr int kNSlices = kConsumers / MT;                // warps sharing one m-tile
   constexpr int kSubPerWarp = (kDecodeStage / 16) / kNSlices;
+  constexpr int kPf = MT == 2 ? 1 : 2;  // shared-memory fragment loads issued this many steps early
 
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -317,43 +328,73 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) decode_split_kernel(
         for (int sb = 0; sb < kSubPerWarp; ++sb)
 #pragma unroll
           for (int j = 0; j < 2; ++j) s[sb][j][0] = s[sb][j][1] = s[sb][j][2] = s[sb][j][3] = 0.f;
-        // S = Q K^T over d
+        // S = Q K^T over d. The inline-asm loads and MMAs keep their source
+        // order, so each step's K fragments are loaded kPf steps ahead of the
+        // MMAs that use them.
         {
           const int mi = lane >> 3;
           const int ri = lane & 7;
-#pragma unroll
-          for (int kk = 0; kk < D / 16; ++kk) {
+          uint32_t fb[kPf + 1][kSubPerWarp][4];
+          auto kfetch = [&](int kk, int buf) {
             const int chunk = (kk * 2 + (mi & 1)) & 7;
 #pragma unroll
             for (int sb = 0; sb < kSubPerWarp; ++sb) {
               if (!act[sb]) continue;
               const int tok = r0[sb] + (mi >> 1) * 8 + ri;
-              const uint32_t addr = kbase + (kk >> 2) * C::kBoxBytes + sw128(tok, chunk);
-              uint32_t b0, b1, b2, b3;
-              ldsm_x4(addr, b0, b1, b2, b3);
-              mma16816(s[sb][0], qa[kk], b0, b1);
-              mma16816(s[sb][1], qa[kk], b2, b3);
+              ldsm_x4(kbase + (kk >> 2) * C::kBoxBytes + sw128(tok, chunk), fb[buf][sb][0],
+                      fb[buf][sb][1], fb[buf][sb][2], fb[buf][sb][3]);
+            }
+          };
+#pragma unroll
+          for (int kk = 0; kk < kPf; ++kk) kfetch(kk, kk);
+#pragma unroll
+          for (int kk = 0; kk < D / 16; ++kk) {
+            if (kk + kPf < D / 16) kfetch(kk + kPf, (kk + kPf) % (kPf + 1));
+            const int bf = kk % (kPf + 1);
+#pragma unroll
+            for (int sb = 0; sb < kSubPerWarp; ++sb) {
+              if (!act[sb]) continue;
+              mma16816(s[sb][0], qa[kk], fb[bf][sb][0], fb[bf][sb][1]);
+              mma16816(s[sb][1], qa[kk], fb[bf][sb][2], fb[bf][sb][3]);
             }
           }
         }
-        // mask, scale to log2 units, online softmax for rows row0 / row1
+        // mask, scale to log2 units, online softmax for rows row0 / row1.
+        // A plain stage (every token of the warp's blocks real, none before the
+        // window, no ALiBi) needs no per-score bias or bound: the max is taken
+        // over the raw scores and the scale goes into the exponent's FMA.
         float mx[2] = {-INFINITY, -INFINITY};
+        bool plain = alibi == nullptr && scale_log2 > 0.f;
 #pragma unroll
         for (int sb = 0; sb < kSubPerWarp; ++sb)
+          plain = plain && act[sb] && r0[sb] + 16 <= valid && r0[sb] >= first;
+        if (plain) {
 #pragma unroll
-          for (int j = 0; j < 2; ++j)
+          for (int sb = 0; sb < kSubPerWarp; ++sb)
 #pragma unroll
-            for (int e = 0; e < 4; ++e) {
-              const int tok = r0[sb] + j * 8 + tq * 2 + (e & 1);
-              // ALiBi: -slope * (query position - key position)
-              const float bias =
-                  slope[e >> 1] * static_cast<float>(tok0 + tok - (it.len - 1));
-              const float x =
-                  act[sb] && tok < valid && tok >= first ? fmaf(s[sb][j][e], scale_log2, bias)
-                                                         : -INFINITY;
-              s[sb][j][e] = x;
-              mx[e >> 1] = fmaxf(mx[e >> 1], x);
-            }
+            for (int j = 0; j < 2; ++j)
+#pragma unroll
+              for (int e = 0; e < 4; ++e) mx[e >> 1] = fmaxf(mx[e >> 1], s[sb][j][e]);
+          mx[0] *= scale_log2;
+          mx[1] *= scale_log2;
+        } else {
+#pragma unroll
+          for (int sb = 0; sb < kSubPerWarp; ++sb)
+#pragma unroll
+            for (int j = 0; j < 2; ++j)
+#pragma unroll
+              for (int e = 0; e < 4; ++e) {
+                const int tok = r0[sb] + j * 8 + tq * 2 + (e & 1);
+                // ALiBi: -slope * (query position - key position)
+                const float bias =
+                    slope[e >> 1] * static_cast<float>(tok0 + tok - (it.len - 1));
+                const float x = act[sb] && tok < valid && tok >= first
+                                    ? fmaf(s[sb][j][e], scale_log2, bias)
+                                    : -INFINITY;
+                s[sb][j][e] = x;
+                mx[e >> 1] = fmaxf(mx[e >> 1], x);
+              }
+        }
         float m_new[2];
 #pragma unroll
         for (int h = 0; h < 2; ++h) {
@@ -382,46 +423,55 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) decode_split_kernel(
         // all-masked so far: keep everything at zero weight
         const float m_use[2] = {m_r[0] == -INFINITY ? 0.f : m_r[0],
                                 m_r[1] == -INFINITY ? 0.f : m_r[1]};
-        // P in bf16 (the A operand of P.V); the row sums add the same rounded
-        // weights, so numerator and denominator round alike
-        float rs[2] = {0.f, 0.f};
+        // P in bf16 (the A operand of P.V), rounded once per pair of one row;
+        // this thread's share of each row sum adds the same rounded weights,
+        // so numerator and denominator round alike (the four shares of a row
+        // are added when the item ends)
+        const float mul = plain ? scale_log2 : 1.f;
+        uint32_t pw[kSubPerWarp][2][2];  // [block][j][row]: two weights of one row
+        float rsa[2] = {0.f, 0.f};
+        float rsb[2] = {0.f, 0.f};
 #pragma unroll
         for (int sb = 0; sb < kSubPerWarp; ++sb)
 #pragma unroll
           for (int j = 0; j < 2; ++j)
 #pragma unroll
-            for (int e = 0; e < 4; ++e) {
-              const float p = __bfloat162float(__float2bfloat16_rn(
-                  ex2_approx(s[sb][j][e] - m_use[e >> 1])));
-              s[sb][j][e] = p;
-              rs[e >> 1] += p;
+            for (int h = 0; h < 2; ++h) {
+              const float e0 = ex2_approx(fmaf(s[sb][j][2 * h], mul, -m_use[h]));
+              const float e1 = ex2_approx(fmaf(s[sb][j][2 * h + 1], mul, -m_use[h]));
+              pw[sb][j][h] = pack_bf16x2(e0, e1);
+              add_bf16x2_to_f32(pw[sb][j][h], rsa[h], rsb[h]);
             }
-#pragma unroll
-        for (int h = 0; h < 2; ++h) {
-          rs[h] += __shfl_xor_sync(0xffffffffu, rs[h], 1);
-          rs[h] += __shfl_xor_sync(0xffffffffu, rs[h], 2);
-          l_r[h] += rs[h];
-        }
-        // P (bf16) as the A fragment of O += P V
-        const int mi = lane >> 3;
-        const int ri = lane & 7;
-#pragma unroll
-        for (int sb = 0; sb < kSubPerWarp; ++sb) {
-          if (!act[sb]) continue;
-          uint32_t pa[4];
-          pa[0] = pack_bf16x2(s[sb][0][0], s[sb][0][1]);
-          pa[1] = pack_bf16x2(s[sb][0][2], s[sb][0][3]);
-          pa[2] = pack_bf16x2(s[sb][1][0], s[sb][1][1]);
-          pa[3] = pack_bf16x2(s[sb][1][2], s[sb][1][3]);
-          const int tok = r0[sb] + (mi & 1) * 8 + ri;
-#pragma unroll
-          for (int np = 0; np < D / 16; ++np) {
+        l_r[0] += rsa[0] + rsb[0];
+        l_r[1] += rsa[1] + rsb[1];
+        // O += P V with P (bf16) as the A fragments; V fragments loaded kPf
+        // steps (of one 16-column pair) ahead of their MMAs
+        {
+          const int mi = lane >> 3;
+          const int ri = lane & 7;
+          constexpr int kSteps = kSubPerWarp * (D / 16);
+          uint32_t vf[kPf + 1][4];
+          auto vfetch = [&](int i, int buf) {
+            const int sb = i / (D / 16);
+            const int np = i % (D / 16);
+            if (!act[sb]) return;
+            const int tok = r0[sb] + (mi & 1) * 8 + ri;
             const int cg = np * 2 + (mi >> 1);
-            const uint32_t addr = vbase + (cg >> 3) * C::kBoxBytes + sw128(tok, cg & 7);
-            uint32_t b0, b1, b2, b3;
-            ldsm_x4_t(addr, b0, b1, b2, b3);
-            mma16816(o_acc[np * 2], pa, b0, b1);
-            mma16816(o_acc[np * 2 + 1], pa, b2, b3);
+            ldsm_x4_t(vbase + (cg >> 3) * C::kBoxBytes + sw128(tok, cg & 7), vf[buf][0],
+                      vf[buf][1], vf[buf][2], vf[buf][3]);
+          };
+#pragma unroll
+          for (int i = 0; i < kPf; ++i) vfetch(i, i);
+#pragma unroll
+          for (int i = 0; i < kSteps; ++i) {
+            if (i + kPf < kSteps) vfetch(i + kPf, (i + kPf) % (kPf + 1));
+            const int sb = i / (D / 16);
+            const int np = i % (D / 16);
+            if (!act[sb]) continue;
+            const uint32_t pa[4] = {pw[sb][0][0], pw[sb][0][1], pw[sb][1][0], pw[sb][1][1]};
+            const int bf = i % (kPf + 1);
+            mma16816(o_acc[np * 2], pa, vf[bf][0], vf[bf][1]);
+            mma16816(o_acc[np * 2 + 1], pa, vf[bf][2], vf[bf][3]);
           }
         }
       }
@@ -436,6 +486,11 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) decode_split_kernel(
       // lse = -inf (weight 0 in the combine)
       {
         const int pslot = it.split * kNSlices + slice;  // partial index within the row
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          l_r[h] += __shfl_xor_sync(0xffffffffu, l_r[h], 1);
+          l_r[h] += __shfl_xor_sync(0xffffffffu, l_r[h], 2);
+        }
 #pragma unroll
         for (int h = 0; h < 2; ++h) {
           const int row = h == 0 ? row0 : row1;
