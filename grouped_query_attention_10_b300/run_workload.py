@@ -2,7 +2,8 @@
 
     python -m grouped_query_attention_10_b300.run_workload <name> [--iters N] [--warmup W]
 
-Names: prefill_tiny, prefill_noncausal, prefill_causal, decode_ragged,
+Names: prefill_tiny, prefill_noncausal, prefill_causal (fp32 output),
+prefill_causal_bf16 (bf16 output, as in the bench step), decode_ragged,
 decode_sweep_g{1,2,4,8,16,32}, append_prompt, and the variants prefill_window
 (W = 1024), prefill_alibi, prefill_kvcache (512 new tokens over 4096),
 decode_paged_p{16,64,256}, decode_window (W = 1024), append_rope. Inputs are the seeded
@@ -43,11 +44,11 @@ def make_l2_flush(dev):
     return flush
 
 
-def _prefill(w, dev, B=None):
+def _prefill(w, dev, B=None, out_dtype=torch.float32):
     if B is not None:
         w = dataclasses.replace(w, B=B)
     q, k, v = inputs.prefill_inputs(w, device=dev)
-    o = torch.empty((w.B, w.L, w.h_q, w.d), dtype=torch.float32, device=dev)
+    o = torch.empty((w.B, w.L, w.h_q, w.d), dtype=out_dtype, device=dev)
     fn = lambda s: gqa.gqa_prefill_fwd(q, k, v, causal=w.causal, scale=w.scale, out=o, stream=s)
     work = accounting.prefill_flops(w.B, w.L, w.h_q, w.d, w.causal)
     return fn, work, "TFLOP/s", 1e12
@@ -169,6 +170,8 @@ def make(name: str, dev, B=None):
         return _prefill(inputs.NONCAUSAL_PREFILL, dev, B)
     if name == "prefill_causal":
         return _prefill(inputs.LLAMA_CAUSAL_PREFILL, dev, B)
+    if name == "prefill_causal_bf16":
+        return _prefill(inputs.LLAMA_CAUSAL_PREFILL, dev, B, out_dtype=torch.bfloat16)
     if name == "decode_ragged":
         return _decode(inputs.DECODE_RAGGED, dev, B)
     if name.startswith("decode_sweep_g"):

@@ -134,10 +134,10 @@ def test_prefill_llama_causal_reduced_length():
     assert_close(f64(o), o_ref, "llama causal prefill, L=1024")
 
 
-def _sampled_prefill_check(w, n_rows, seed):
+def _sampled_prefill_check(w, n_rows, seed, out_dtype=torch.float32):
     q, k, v = inputs.prefill_inputs(w, device=DEV)
     lse = torch.empty((w.B, w.h_q, w.L), dtype=torch.float32, device=DEV)
-    o = gqa.gqa_prefill_fwd(q, k, v, causal=w.causal, scale=w.scale, lse=lse)
+    o = gqa.gqa_prefill_fwd(q, k, v, causal=w.causal, scale=w.scale, lse=lse, out_dtype=out_dtype)
     torch.cuda.synchronize()
     rng = np.random.default_rng(seed)
     rows = [(int(rng.integers(w.B)), int(rng.integers(w.L))) for _ in range(n_rows)]
@@ -161,6 +161,12 @@ def test_prefill_noncausal_workload_full_size_sampled():
 
 def test_prefill_llama_causal_workload_full_size_sampled():
     _sampled_prefill_check(inputs.LLAMA_CAUSAL_PREFILL, 24, seed=6)
+
+
+def test_prefill_llama_causal_workload_full_size_sampled_bf16_output():
+    # the launch configuration the bench step times: bf16 output (the input
+    # dtype), fp32 accumulation; the output's own rounding is inside the bound
+    _sampled_prefill_check(inputs.LLAMA_CAUSAL_PREFILL, 24, seed=7, out_dtype=torch.bfloat16)
 
 
 # ---------------------------------------------------------------------------

@@ -5,7 +5,8 @@ whose memory planner owns every allocation, serving loops that must not call
 cudaMalloc once running -- from a scratch array built into the library. These
 tests call it through the C interface and check that its results match
 gqa_decode_fwd (which takes a caller-allocated workspace) on two calls in a
-row, the second reusing the scratch left behind by the first.
+row, the second reusing the scratch left behind by the first, and that they
+match the fp64 oracle's decode.
 
 This file is named so that pytest collects it last.
 """
@@ -15,6 +16,8 @@ import ctypes
 import pytest
 import torch
 
+import numpy as np
+import oracle
 from grouped_query_attention_10_b300 import binding
 from grouped_query_attention_10_b300 import inputs
 
@@ -94,3 +97,30 @@ def test_noalloc_matches_workspace_entry_point_twice(lib):
     _case(lib, B=8, h_q=32, g=8, d=128, S_max=2048, seed=501, lens_override=[0, 1, 2048, 777])
     # second call in a row: other sizes, reusing the scratch the first call left
     _case(lib, B=3, h_q=16, g=2, d=64, S_max=3000, seed=502, lens_override=[3000, 65])
+
+
+@pytest.mark.gpu
+def test_noalloc_matches_the_oracle(lib):
+    dev = torch.device("cuda", 0)
+    B, h_q, g, d, S_max = 4, 32, 8, 128, 1000
+    w = inputs.DecodeWorkload("noalloc_oracle", B=B, h_q=h_q, g=g, d=d, S_max=S_max,
+                              len_lo=1, len_hi=S_max, seed=503)
+    q, kc, vc, lens = (t.to(dev) for t in inputs.decode_inputs(w))
+    lens_l = [1000, 1, 517, 64]
+    lens[:] = torch.tensor(lens_l, dtype=torch.int32)
+    scale = 1.0 / d ** 0.5
+    o = torch.full((B, h_q, d), float("nan"), dtype=torch.float32, device=dev)
+    lse = torch.full((B, h_q), float("nan"), dtype=torch.float32, device=dev)
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    torch.cuda.synchronize()
+    rc = _noalloc(lib, q.data_ptr(), kc.data_ptr(), vc.data_ptr(), lens.data_ptr(), o.data_ptr(),
+                  lse.data_ptr(), B, h_q, g, d, S_max, ctypes.c_float(scale), status.data_ptr())
+    torch.cuda.synchronize()
+    assert rc == binding.GQA_OK, binding.status_string(rc)
+    assert int(status.item()) == 0
+    f64 = lambda t: t.detach().to(torch.float64).cpu().numpy()
+    o_ref, lse_ref = oracle.decode(f64(q), f64(kc), f64(vc), lens_l, scale)
+    for got, ref, what in ((f64(o), o_ref, "O"), (f64(lse), lse_ref, "lse")):
+        err = np.abs(got - ref)
+        assert err.max() <= MAX_ABS, f"noalloc {what} vs oracle: max abs err {err.max():.3e}"
+        assert err.mean() <= MEAN_ABS, f"noalloc {what} vs oracle: mean abs err {err.mean():.3e}"
