@@ -777,7 +777,7 @@ def reference_arm(args):
         "dtype": "f64",
         "data": "synthetic (seeded N(0,1) bf16)",
         "config": {"workload": w.name, "B": w.B, "L": w.L, "h_q": w.h_q, "g": w.g, "d": w.d,
-                   "causal": True, "parallelism": "cpu, rank 0 only"},
+                   "causal": True, "out": "f64 (the oracle)", "parallelism": "cpu, rank 0 only"},
         "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": blas_threads(),
                          "kind": "oracle", "cpu": cpu_model(),
                          "sample": f"fp64 NumPy oracle, one block of {rows} causal query rows "

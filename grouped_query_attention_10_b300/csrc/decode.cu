@@ -297,8 +297,9 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) decode_split_kernel(
       const uint32_t kbase = smem_base + slot * C::kStageBytes;
       const uint32_t vbase = kbase + kCB * C::kBoxBytes;
       // This warp's 16-token blocks of the stage are processed together (their
-      // score products form independent MMA chains), with one max / sum
-      // reduction and one rescale decision for all of them.
+      // score products form independent MMA chains), with one max reduction
+      // and one rescale decision for all of them (the row sums are kept per
+      // thread and reduced once per item).
       int r0[kSubPerWarp];
       bool act[kSubPerWarp];
 #pragma unroll

@@ -202,7 +202,10 @@ int gqa_decode_fwd_ex(const void* q, const void* k_cache, const void* v_cache,
  * Token t of sequence b is copied bit for bit into row seq_lens[b] + t of
  * every K/V head. Rows that would land at or past S_max are dropped and
  * GQA_ERR_CACHE_FULL is recorded in *status_dev (if given). Two launches are
- * queued: the row copy, then the length update.
+ * queued: the row copy, then the length update. The update is a programmatic
+ * dependent launch that may start once every row-copy block has read its
+ * lengths, before the copied rows have landed; later work on the stream sees
+ * both complete, as with any two launches.
  */
 int kv_cache_append(void* k_cache, void* v_cache, int32_t* seq_lens,
                     const void* k_new, const void* v_new, int B, int g, int d,
