@@ -707,9 +707,12 @@ def extra_measurements(dev, stream, peaks, peak_src, flush):
         prep = flush if reset is None else (lambda: (reset(), flush()))
         _time_calls(call, 3, stream, prep)
         ts = _time_calls(call, n, stream, prep)
-        t = statistics.mean(ts)
+        # the median call (a context figure robust to an occasional slow call);
+        # the mean beside it
+        t = statistics.median(ts)
         rate = work / t / div
-        rec = {"rate": round(rate, 2), "unit": unit, "us": round(t * 1e6, 2)}
+        rec = {"rate": round(rate, 2), "unit": unit, "us": round(t * 1e6, 2),
+               "mean_us": round(statistics.mean(ts) * 1e6, 2), "timed": f"median of {n} calls"}
         if unit == "TFLOP/s":
             rec["frac_of_bf16_peak"] = round(rate / peaks["bf16_tflops"], 4)
             rec["frac_of_nominal"] = round(rate / NOMINAL_BF16_TFLOPS, 4)
@@ -728,6 +731,11 @@ def extra_measurements(dev, stream, peaks, peak_src, flush):
         out[f"decode_sweep_b16_hq32_g{g}_d128_s32768"] = one(f"decode_sweep_g{g}", 20)
     for name in ("prefill_window", "prefill_alibi", "prefill_kvcache", "decode_paged_p16",
                  "decode_paged_p64", "decode_window", "append_prompt", "append_rope"):
+        out[name] = one(name, 20)
+    # the prefill workloads above write fp32 output; the same with bf16 output
+    # (the input dtype, as in the step)
+    for name in ("prefill_noncausal_bf16", "prefill_window_bf16", "prefill_alibi_bf16",
+                 "prefill_kvcache_bf16"):
         out[name] = one(name, 20)
     return out
 

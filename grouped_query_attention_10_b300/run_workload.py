@@ -7,7 +7,9 @@ prefill_causal_bf16 (bf16 output, as in the bench step), decode_ragged,
 decode_sweep_g{1,2,4,8,16,32}, append_prompt, and the variants prefill_window
 (W = 1024), prefill_alibi, prefill_kvcache (512 new tokens over 4096),
 decode_paged_p{16,64,256}, decode_window (W = 1024), append_rope. Inputs are the seeded
-synthetic workloads of ``inputs.py``. Each timed call is bracketed by CUDA
+synthetic workloads of ``inputs.py``. The prefill workloads write fp32 output;
+prefill_{noncausal,window,alibi,kvcache}_bf16 are the same with bf16 output.
+Each timed call is bracketed by CUDA
 events on the launching stream; an L2 flush precedes every call (a 256 MiB
 write, then a 256 MiB read of another buffer, so the write's dirty lines are
 written back before the timed call starts). The append workloads write into
@@ -81,11 +83,11 @@ def _append(dev):
     return fn, accounting.append_bytes(w.B, w.L, w.g, w.d), "GB/s", 1e9
 
 
-def _prefill_variant(dev, window=0, alibi=False):
+def _prefill_variant(dev, window=0, alibi=False, out_dtype=torch.float32):
     """The causal Llama-shape prefill with a sliding window or ALiBi slopes."""
     w = inputs.LLAMA_CAUSAL_PREFILL
     q, k, v = inputs.prefill_inputs(w, device=dev)
-    o = torch.empty((w.B, w.L, w.h_q, w.d), dtype=torch.float32, device=dev)
+    o = torch.empty((w.B, w.L, w.h_q, w.d), dtype=out_dtype, device=dev)
     slopes = (torch.tensor([2.0 ** (-8.0 * (h + 1) / w.h_q) for h in range(w.h_q)],
                            dtype=torch.float32, device=dev) if alibi else None)
     fn = lambda s: gqa.gqa_prefill_fwd(q, k, v, causal=True, scale=w.scale, out=o, stream=s,
@@ -95,7 +97,7 @@ def _prefill_variant(dev, window=0, alibi=False):
     return fn, work, "TFLOP/s", 1e12
 
 
-def _prefill_kvcache(dev, T=512):
+def _prefill_kvcache(dev, T=512, out_dtype=torch.float32):
     """Chunked prefill: the last T of 4096 tokens per sequence of the Llama
     shape attend to the whole cache."""
     w = inputs.LLAMA_CAUSAL_PREFILL
@@ -104,7 +106,7 @@ def _prefill_kvcache(dev, T=512):
     vc = v.transpose(1, 2).contiguous()
     qn = q[:, w.L - T:].contiguous()
     lens = torch.full((w.B,), w.L, dtype=torch.int32, device=dev)
-    o = torch.empty((w.B, T, w.h_q, w.d), dtype=torch.float32, device=dev)
+    o = torch.empty((w.B, T, w.h_q, w.d), dtype=out_dtype, device=dev)
     fn = lambda s: gqa.gqa_prefill_kvcache_fwd(qn, kc, vc, lens, scale=w.scale, out=o, stream=s)
     return fn, accounting.prefill_cached_flops([w.L] * w.B, T, w.h_q, w.d), "TFLOP/s", 1e12
 
@@ -164,6 +166,19 @@ def _append_rope(dev):
 
 
 def make(name: str, dev, B=None):
+    if name.endswith("_bf16") and name != "prefill_causal_bf16":
+        # the same workload with bf16 output (the input dtype)
+        base = name[:-len("_bf16")]
+        bf = torch.bfloat16
+        if base == "prefill_noncausal":
+            return _prefill(inputs.NONCAUSAL_PREFILL, dev, B, out_dtype=bf)
+        if base == "prefill_window":
+            return _prefill_variant(dev, window=1024, out_dtype=bf)
+        if base == "prefill_alibi":
+            return _prefill_variant(dev, alibi=True, out_dtype=bf)
+        if base == "prefill_kvcache":
+            return _prefill_kvcache(dev, out_dtype=bf)
+        raise SystemExit(f"unknown workload {name}")
     if name == "prefill_tiny":
         return _prefill(inputs.TINY_CAUSAL_PREFILL, dev, B)
     if name == "prefill_noncausal":

@@ -101,6 +101,26 @@ def test_prefill_alibi(d, causal, h_q, g):
     assert_close(f64(lse), lse_ref, "lse")
 
 
+@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("window", [0, 200])
+def test_prefill_alibi_window_bf16_output(d, window):
+    # the variant instantiations through the bf16-output epilogue, guarded
+    B, L, h_q, g = 2, 300, 16, 4
+    q = rand_bf16((B, L, h_q, d), 450 + window + d)
+    k = rand_bf16((B, L, g, d), 451 + window + d)
+    v = rand_bf16((B, L, g, d), 452 + window + d)
+    scale = 1.0 / math.sqrt(d)
+    slopes = alibi_slopes(h_q)
+    go = guard.empty((B, L, h_q, d), torch.bfloat16, DEV)
+    o = gqa.gqa_prefill_fwd(q, k, v, causal=True, scale=scale, window=window,
+                            alibi_slopes=slopes, out=go.tensor)
+    torch.cuda.synchronize()
+    go.assert_bands("ALiBi/window prefill bf16 O")
+    o_ref, _ = oracle.prefill(f64(q), f64(k), f64(v), True, scale, window=window,
+                              alibi_slopes=slopes.cpu().numpy().astype(np.float64))
+    assert_close(f64(o), o_ref, f"alibi window={window} d={d} bf16 output")
+
+
 def test_prefill_window_and_alibi_llama_shape_sampled_rows():
     B, L, h_q, g, d, W = 2, 2048, 32, 8, 128, 512
     q = rand_bf16((B, L, h_q, d), 501)
@@ -135,7 +155,8 @@ def test_prefill_window_wider_than_sequence_equals_plain_causal():
 # chunked prefill over the KV cache
 # ---------------------------------------------------------------------------
 
-def _cached_case(B, T, h_q, g, d, S_max, lens, seed, window=0, alibi=False, nan_tail=True):
+def _cached_case(B, T, h_q, g, d, S_max, lens, seed, window=0, alibi=False, nan_tail=True,
+                 out_dtype=torch.float32):
     kc = rand_bf16((B, g, S_max, d), seed)
     vc = rand_bf16((B, g, S_max, d), seed + 1)
     q = rand_bf16((B, T, h_q, d), seed + 2)
@@ -146,7 +167,7 @@ def _cached_case(B, T, h_q, g, d, S_max, lens, seed, window=0, alibi=False, nan_
             vc[b, :, n:] = float("nan")
     slopes = alibi_slopes(h_q) if alibi else None
     scale = 1.0 / math.sqrt(d)
-    go = guard.empty((B, T, h_q, d), torch.float32, DEV)
+    go = guard.empty((B, T, h_q, d), out_dtype, DEV)
     gl = guard.empty((B, h_q, T), torch.float32, DEV)
     lse = gl.tensor
     status = torch.zeros(1, dtype=torch.int32, device=DEV)
@@ -180,6 +201,15 @@ def test_prefill_kvcache_variants(h_q, g, window, alibi):
     o, lse, o_ref, lse_ref = _cached_case(2, 100, h_q, g, 128, 900, [900, 333], seed=700 + h_q,
                                           window=window, alibi=alibi)
     assert_close(f64(o), o_ref, f"kvcache window={window} alibi={alibi}")
+    assert_close(f64(lse), lse_ref, "lse")
+
+
+@pytest.mark.parametrize("d", [64, 128])
+def test_prefill_kvcache_bf16_output(d):
+    o, lse, o_ref, lse_ref = _cached_case(3, 129, 32, 8, d, 1024, [129, 600, 1024], seed=750 + d,
+                                          out_dtype=torch.bfloat16)
+    assert o.dtype == torch.bfloat16
+    assert_close(f64(o), o_ref, f"kvcache bf16 output d={d}")
     assert_close(f64(lse), lse_ref, "lse")
 
 
