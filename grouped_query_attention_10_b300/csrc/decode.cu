@@ -16,7 +16,10 @@
 //    per query head. Every item ends with its normalised partial output and
 //    its log2 sum-exp.
 //  * pass 2 (decode_combine_kernel): log-sum-exp combine of the partials,
-//    launched as a programmatic dependent of pass 1.
+//    launched as a programmatic dependent of pass 1. When every sequence's
+//    rows (or window) fit one split, pass 1 merges the partials of each item
+//    itself, right after its consumer warps have written them, and writes the
+//    output; pass 2 is not launched.
 #include <cuda_bf16.h>
 
 #include "../../include/gqa.h"
@@ -128,6 +131,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) decode_split_kernel(
     int n_hslice, int S_max, int split_len, int n_split, int n_items, float scale_log2,
     int window, const float* __restrict__ alibi, const int32_t* __restrict__ block_table,
     int page_log2, int num_pages, int max_blocks, int* __restrict__ item_counter,
+    void* __restrict__ o_out, int o_dtype, float* __restrict__ lse_out, int fused,
     int32_t* status) {
   using C = DecCfg<D>;
   constexpr int kStages = C::kStages;
@@ -143,6 +147,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) decode_split_kernel(
   __shared__ __align__(8) uint64_t empty_bar[kStages];   // one arrival per consumer warp
   __shared__ int4 tag[kStages];              // item, stage, stages of the item (item < 0: end)
   __shared__ int abort_flag;
+  __shared__ __align__(8) uint64_t merge_bar;  // the consumer warps' partials of an item written
 
   const int tid = threadIdx.x;
   const int warp = tid >> 5;
@@ -154,6 +159,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) decode_split_kernel(
       mbar_init(&full_bar[i], 1);
       mbar_init(&empty_bar[i], kConsumers);
     }
+    mbar_init(&merge_bar, kConsumers);
     fence_mbar_init();
   }
   __syncthreads();
@@ -172,6 +178,28 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) decode_split_kernel(
            u = atomicAdd(item_counter, 1)) {
         const Item it = decode_item(u, seq_lens, g, n_hslice, S_max, split_len, n_segs, window);
         const int zrow = it.b * g + it.kvh;
+        if (fused && it.split == 0) {
+          // no combine runs to flag a bad length: flag it here
+          const int raw = seq_lens[it.b];
+          if ((raw < 0 || raw > S_max) && it.kvh == 0 && it.hs == 0)
+            record_status(status, GQA_ERR_BAD_LENGTH);
+        }
+        if (fused && it.n_st == 0 && it.split == 0) {
+          // a sequence with no rows: its output rows are zero, lse -inf
+          const size_t h0 = static_cast<size_t>(it.b) * h_q + static_cast<size_t>(it.kvh) * G +
+                            it.hs * 32;
+          const int gs = min(G - it.hs * 32, 16 * MT);
+          for (int r = 0; r < gs; ++r) {
+            for (int c = 0; c < D; ++c) {
+              if (o_dtype == GQA_OUT_F32)
+                static_cast<float*>(o_out)[(h0 + r) * D + c] = 0.f;
+              else
+                static_cast<__nv_bfloat16*>(o_out)[(h0 + r) * D + c] =
+                    __float2bfloat16_rn(0.f);
+            }
+            if (lse_out != nullptr) lse_out[h0 + r] = -INFINITY;
+          }
+        }
         for (int st = 0; st < it.n_st; ++st, ++sc) {
           const int slot = sc % kStages;
           if (sc >= kStages) ok = mbar_wait(&empty_bar[slot], ((sc / kStages) - 1) & 1, &abort_flag);
@@ -251,6 +279,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) decode_split_kernel(
     Item it{};
     size_t head0 = 0;
     int Gs = 0;
+    int n_merged = 0;  // items merged by this CTA (merge_bar phases)
     uint32_t qa[D / 16][4];
     float o_acc[D / 8][4];
     float m_r[2] = {-INFINITY, -INFINITY};  // running max (log2 units), stale by < 2^8
@@ -507,6 +536,46 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) decode_split_kernel(
           if (tq == 0) part_lse[ps] = any ? m_r[h] + __log2f(l_r[h]) : -INFINITY;
         }
       }
+      if (fused) {
+        // one split per segment: every consumer warp has written its slice's
+        // partial of this item; merge them and write the output rows here
+        __threadfence_block();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&merge_bar);
+        ok = __all_sync(0xffffffffu, mbar_wait(&merge_bar, n_merged & 1, &abort_flag));
+        ++n_merged;
+        if (!ok) break;
+        constexpr int kCols = D / 4;               // columns per warp
+        constexpr int kRowStep = 32 / kCols;       // rows per pass of the warp
+        const int c = warp * kCols + lane % kCols;
+        const size_t n_part = static_cast<size_t>(n_split) * kNSlices;
+        for (int r = lane / kCols; r < Gs; r += kRowStep) {
+          const size_t pr = (head0 + r) * n_part + it.split * kNSlices;
+          float ls[kNSlices];
+          float mx = -INFINITY;
+#pragma unroll
+          for (int s2 = 0; s2 < kNSlices; ++s2) {
+            ls[s2] = part_lse[pr + s2];
+            mx = fmaxf(mx, ls[s2]);
+          }
+          const float mm = mx == -INFINITY ? 0.f : mx;
+          float den = 0.f, acc = 0.f;
+#pragma unroll
+          for (int s2 = 0; s2 < kNSlices; ++s2) {
+            const float w = ex2_approx(ls[s2] - mm);
+            den += w;
+            acc += w * part_o[(pr + s2) * D + c];
+          }
+          const float out = den > 0.f ? acc / den : 0.f;
+          if (o_dtype == GQA_OUT_F32)
+            static_cast<float*>(o_out)[(head0 + r) * D + c] = out;
+          else
+            static_cast<__nv_bfloat16*>(o_out)[(head0 + r) * D + c] = __float2bfloat16_rn(out);
+          if (lse_out != nullptr && c == 0)
+            lse_out[head0 + r] =
+                den > 0.f ? (mm + __log2f(den)) * 0.69314718055994531f : -INFINITY;
+        }
+      }
     }
   }
   __syncthreads();
@@ -655,6 +724,11 @@ static cudaError_t launch_decode_t(const DecodeArgs& a, cudaStream_t s) {
   const long long n_items = static_cast<long long>(a.B) * a.g * n_hslice * a.n_split;
   const long long slots = static_cast<long long>(device_sm_count()) * kCtasPerSm;
   const int grid = static_cast<int>(n_items < slots ? n_items : slots);
+  // every segment's rows (a window: its rows plus up to 63 before it in its
+  // first stage) fit one split: the split pass writes the output itself
+  const long long w_rows = a.window < a.S_max ? a.window : a.S_max;
+  const long long rows_max = a.window > 0 ? w_rows + kDecodeStage - 1 : a.S_max;
+  const bool fused = rows_max <= a.split_len;
   // the item counter the persistent CTAs fetch from starts at zero
   e = cudaMemsetAsync(a.item_counter, 0, sizeof(int), s);
   if (e != cudaSuccess) return e;
@@ -662,9 +736,10 @@ static cudaError_t launch_decode_t(const DecodeArgs& a, cudaStream_t s) {
       a.tm_k, a.tm_v, static_cast<const __nv_bfloat16*>(a.q), a.seq_lens, a.part_o, a.part_lse,
       a.h_q, a.g, a.G, n_hslice, a.S_max, a.split_len, a.n_split, static_cast<int>(n_items),
       a.scale_log2, a.window, a.alibi, a.block_table, a.page_log2, a.num_pages, a.max_blocks,
-      a.item_counter, a.status);
+      a.item_counter, a.o, a.o_dtype, a.lse, fused ? 1 : 0, a.status);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
+  if (fused) return cudaSuccess;
   // The combine is a programmatic dependent launch: its CTAs are scheduled
   // while the split pass drains and block in griddepcontrol.wait until it
   // has finished, which hides most of the launch gap between the two.

@@ -347,6 +347,52 @@ def test_decode_window_longer_than_the_cache_with_few_segments():
     assert_close(f64(o), o_ref, "window > cache, few segments")
 
 
+@pytest.mark.parametrize("window", [0, 300])
+@pytest.mark.parametrize("out_dtype", [torch.float32, torch.bfloat16])
+@pytest.mark.parametrize("B,h_q,g,d,S_max", [(40, 32, 8, 128, 1500), (240, 32, 1, 128, 256),
+                                             (40, 8, 8, 64, 700)])
+def test_decode_single_split_writes_the_output(window, out_dtype, B, h_q, g, d, S_max):
+    # enough (sequence, K/V head) segments to fill the CTA slots with one split
+    # each and a cache that fits one split: the split pass merges its consumer
+    # warps' partials and writes O and lse itself (no combine pass). Empty
+    # sequences, one-row and full ones, NaN rows past the lengths.
+    kc = rand_bf16((B, g, S_max, d), 1400 + B + g)
+    vc = rand_bf16((B, g, S_max, d), 1401 + B + g)
+    q = rand_bf16((B, h_q, d), 1402 + B + g)
+    gen = torch.Generator().manual_seed(1403 + B)
+    lens_l = torch.randint(0, S_max + 1, (B,), generator=gen).tolist()
+    lens_l[:5] = [0, 1, S_max, 63, 65 if S_max > 65 else S_max]
+    for b, n in enumerate(lens_l):
+        kc[b, :, n:] = float("nan")
+        vc[b, :, n:] = float("nan")
+    go = guard.empty((B, h_q, d), out_dtype, DEV)
+    gl = guard.empty((B, h_q), torch.float32, DEV)
+    status = torch.zeros(1, dtype=torch.int32, device=DEV)
+    gqa.gqa_decode_fwd(q, kc, vc, torch.tensor(lens_l, dtype=torch.int32, device=DEV),
+                       scale=0.1, window=window, lse=gl.tensor, out=go.tensor, status=status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    go.assert_bands("single-split decode O")
+    gl.assert_bands("single-split decode lse")
+    o_ref, lse_ref = oracle.decode(f64(q), np.nan_to_num(f64(kc)), np.nan_to_num(f64(vc)),
+                                   lens_l, 0.1, window=window)
+    assert_close(f64(go.tensor), o_ref, f"single-split decode B={B} g={g} window={window}")
+    assert_close(f64(gl.tensor), lse_ref, "single-split decode lse")
+
+
+def test_decode_single_split_flags_a_bad_length():
+    B, h_q, g, d, S_max = 40, 32, 8, 128, 1000
+    kc = rand_bf16((B, g, S_max, d), 1501)
+    vc = rand_bf16((B, g, S_max, d), 1502)
+    q = rand_bf16((B, h_q, d), 1503)
+    lens = torch.full((B,), 500, dtype=torch.int32, device=DEV)
+    lens[7] = -3
+    status = torch.zeros(1, dtype=torch.int32, device=DEV)
+    gqa.gqa_decode_fwd(q, kc, vc, lens, status=status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == gqa.GQA_ERR_BAD_LENGTH
+
+
 def test_decode_equals_one_token_chunked_prefill_with_bias():
     B, h_q, g, d, S_max = 3, 32, 8, 128, 1500
     kc = rand_bf16((B, g, S_max, d), 1101)
