@@ -71,16 +71,21 @@ __global__ void __launch_bounds__(256) kv_append_rows_kernel(
 // Advance every valid length by T, saturating at S_max. After the K/V row
 // copies it is launched as a programmatic dependent: it starts once every
 // row-copy CTA has read its lengths (lengths_read), so no row-copy thread can
-// observe the new length; the row stores may still be in flight, and the next
-// operation on the stream waits for both kernels as usual. After the RoPE
-// append it runs in plain stream order.
+// observe the new length, and writes the lengths while the row stores may
+// still be in flight. It then waits (griddepcontrol.wait) for the row copy to
+// complete before it exits: work queued after the append is ordered after
+// this kernel, and so after the copy as well. After the RoPE append it runs
+// in plain stream order (the wait is then a no-op).
 __global__ void kv_append_lens_kernel(int32_t* seq_lens, int B, int S_max, int T) {
   const int b = blockIdx.x * blockDim.x + threadIdx.x;
-  if (b >= B) return;
-  const int len = seq_lens[b];
-  if (len < 0 || len > S_max) return;  // flagged by the row kernel, left as is
-  const long long n = static_cast<long long>(len) + T;
-  seq_lens[b] = static_cast<int32_t>(n < S_max ? n : S_max);
+  if (b < B) {
+    const int len = seq_lens[b];
+    if (len >= 0 && len <= S_max) {  // a bad length is flagged by the row kernel, left as is
+      const long long n = static_cast<long long>(len) + T;
+      seq_lens[b] = static_cast<int32_t>(n < S_max ? n : S_max);
+    }
+  }
+  asm volatile("griddepcontrol.wait;" ::: "memory");
 }
 
 static cudaError_t launch_lens_update(int32_t* seq_lens, int B, int cap, int T, cudaStream_t s) {
